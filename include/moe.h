@@ -1,0 +1,192 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) MoE layer hot path.
+ *
+ * One Mixture-of-Experts layer on one GPU, in the four steps the Ultralytics
+ * glossary page "Expert Parallelism" gives in its section "How tokens move between
+ * GPUs" (German edition: "Wie Tokens zwischen GPUs uebertragen werden"):
+ *   1. routing   -- moe_route       score every expert per token, keep the top k
+ *   2. dispatch  -- moe_dispatch    count, cap, and permute hidden states into the
+ *                                   contiguous per-expert (per-rank) send layout
+ *   3. compute   -- moe_expert_ffn  run each expert on the rows it received
+ *   4. combine   -- moe_combine     return outputs to token order, weighted by the
+ *                                   router scores, and sum
+ * plus the bias-based balancing step of the section "Load balancing and capacity"
+ * (moe_bias_update).  Expert-parallel ranks are logical only: the expert -> rank
+ * map yields the per-rank counts and offsets an all-to-all would use as its splits;
+ * nothing leaves the GPU.
+ *
+ * Conventions (all calls):
+ *   - Every pointer argument is a DEVICE pointer unless its comment says "host".
+ *     The caller allocates and owns every buffer; no call allocates device memory.
+ *     Scratch memory comes only from the caller's workspace (moe_workspace_size).
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  No call synchronises the host and
+ *     nothing is read back to the host: counts stay on the device.
+ *   - Arguments are validated on the host before anything is launched; a rejected
+ *     call launches nothing and returns MOE_ERR_INVALID_ARG (bad sizes, null or
+ *     misaligned pointers), MOE_ERR_WORKSPACE (workspace too small),
+ *     MOE_ERR_UNSUPPORTED (device is not compute capability 10.3).  A failed
+ *     launch returns MOE_ERR_CUDA.  No exception crosses this interface.
+ *   - Activation buffers (x, xperm, yperm, yshared, out, expert weights) have the
+ *     element type cfg->act_dtype and must be 16-byte aligned; `hidden` and `d_ff`
+ *     must be multiples of 8.  Row-major throughout.
+ *   - Router logits must be finite; NaN logits give unspecified routing.
+ *   - Buffers written by one call must not alias buffers it reads.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_WORKSPACE = 3,
+  MOE_ERR_CUDA = 4
+} moe_status;
+
+enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 };
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum { MOE_RANK_CONTIGUOUS = 0, MOE_RANK_ROUND_ROBIN = 1 };
+
+/* Layer configuration (host struct, passed by const pointer; read during the call
+ * only).  Limits: 1 <= tokens; 8 <= hidden, hidden % 8 == 0;
+ * 1 <= num_experts <= 256; 1 <= top_k <= min(8, num_experts);
+ * 1 <= num_ranks <= num_experts (num_experts % num_ranks == 0 for the contiguous
+ * map); num_groups divides num_experts; 1 <= topk_groups <= num_groups and
+ * topk_groups * (num_experts / num_groups) >= top_k; d_ff >= 8, d_ff % 8 == 0;
+ * shared_d_ff == 0 or a multiple of 8. */
+typedef struct {
+  int32_t tokens;          /* N: tokens in the batch */
+  int32_t hidden;          /* d: hidden size of a token */
+  int32_t num_experts;     /* E: routed experts */
+  int32_t top_k;           /* k: experts kept per token */
+  int32_t num_ranks;       /* R: logical expert-parallel ranks ("GPUs" on the page) */
+  int32_t rank_map;        /* MOE_RANK_CONTIGUOUS: rank = e / (E/R) (experts 0..E/R-1 on
+                              rank 0, as in the page's example); MOE_RANK_ROUND_ROBIN:
+                              rank = e % R */
+  int32_t score_fn;        /* MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID (+ selection bias) */
+  int32_t normalize_topk;  /* nonzero: combine weights renormalised over the k kept */
+  int32_t num_groups;      /* expert groups (one per node); 1 = no group limit */
+  int32_t topk_groups;     /* groups a token may use; 1 when num_groups == 1 */
+  float capacity_factor;   /* > 0: per-expert cap C = ceil(cf * N * k / E); <= 0: none */
+  int32_t d_ff;            /* F: routed expert intermediate size */
+  int32_t shared_d_ff;     /* Fs: always-on shared expert size, 0 = none */
+  int32_t act_dtype;       /* MOE_DTYPE_F32 or MOE_DTYPE_BF16 (activations and expert
+                              weights); the router weight and logits are always fp32 */
+} moe_config;
+
+/* Bytes of workspace that every call below needs for `cfg` (one size serves all
+ * calls; a larger workspace is fine).  `bytes` is a HOST pointer.  The workspace is
+ * device memory, 256-byte aligned, owned by the caller; its contents on entry do not
+ * matter and on exit are unspecified.  Calls sharing one workspace must not overlap
+ * on the GPU. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Routing.  Ultralytics glossary "Expert Parallelism", section "How tokens move
+ * between GPUs", step 1 (the router scores each token against every expert and keeps
+ * the k best) and step 4 (outputs are weighted by the router scores); section "Load
+ * balancing and capacity" (a per-expert bias added to the scores changes only which
+ * experts are selected; each token reaches experts on at most 4 of 8 nodes).
+ *
+ *   x         [N, d]  act_dtype   hidden states
+ *   w_router  [E, d]  fp32        router weight (nn.Linear layout)
+ *   b_router  [E]     fp32        router bias, or NULL
+ *   sel_bias  [E]     fp32        selection-only bias (sigmoid scoring), or NULL
+ *   logits    [N, E]  fp32        out: x . w_router^T + b_router (fp32-accurate)
+ *   topk_idx  [N, k]  int32       out: selected experts, best first
+ *   topk_w    [N, k]  fp32        out: combine weights
+ * Softmax: experts are ranked by logit; weight = softmax probability over all E
+ * (renormalised over the k kept if normalize_topk).  Sigmoid: s = S(logit) (a fixed
+ * fp32 sigmoid), ranked by s + sel_bias; weight = s (no bias), renormalised over the
+ * k kept if normalize_topk.  Group limit: group score = sum of the two best ranking
+ * keys in the group; only the topk_groups best groups are eligible.  Ties break
+ * toward the lower expert / group index. */
+moe_status moe_route(const moe_config* cfg, const void* x, const float* w_router,
+                     const float* b_router, const float* sel_bias, float* logits,
+                     int32_t* topk_idx, float* topk_w, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Dispatch.  Same page, step 2 (each token's hidden state goes to the rank holding
+ * its expert) and the page's counting example (assignments per expert and per
+ * device); section "Load balancing and capacity" (capacity factor: an expert takes
+ * at most cf times its even share, overflow skips that expert).  Deterministic:
+ * assignments a = t*k + j are processed in token order.
+ *
+ *   topk_idx      [N, k]     int32      from moe_route
+ *   x             [N, d]     act_dtype  hidden states
+ *   xperm         [N*k, d]   act_dtype  out: send buffer, rows [0, num_kept) written,
+ *                                       ordered by rank, then expert, then token
+ *   expert_counts [E]        int32      out: routed assignments per expert (pre-cap)
+ *   kept_counts   [E]        int32      out: min(count, C)
+ *   expert_start  [E]        int32      out: first xperm row of each expert
+ *   rank_counts   [R]        int32      out: kept rows per logical rank
+ *   rank_offsets  [R + 1]    int32      out: exclusive prefix of rank_counts
+ *   slot_of       [N*k]      int32      out: xperm row of assignment a, -1 if dropped
+ *   perm_src      [N*k]      int32      out: assignment held by xperm row s
+ *                                       (s < num_kept), -1 for s >= num_kept
+ *   num_kept      [1]        int32      out: rows written to xperm
+ * xperm may be NULL to compute the routing tables only (x is then ignored). */
+moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                        void* xperm, int32_t* expert_counts, int32_t* kept_counts,
+                        int32_t* expert_start, int32_t* rank_counts, int32_t* rank_offsets,
+                        int32_t* slot_of, int32_t* perm_src, int32_t* num_kept,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Expert compute.  Same page, step 3 (each rank runs its local experts on the
+ * tokens it received); fudan-mlsys-cn chapter 10, section 10.5 (a shared expert sees
+ * every token).  Each expert is a SwiGLU feed-forward block:
+ *   h = silu(X Wg^T) * (X Wu^T),  Y = h Wd^T
+ *
+ *   xperm          [N*k, d]       act_dtype  from moe_dispatch
+ *   expert_start   [E], kept_counts [E]  int32  from moe_dispatch (read on device)
+ *   w_gate_up      [E, 2F, d]     act_dtype  rows 0..F-1 gate Wg, F..2F-1 up Wu
+ *   w_down         [E, d, F]      act_dtype  Wd
+ *   x              [N, d]         act_dtype  input of the shared expert (NULL if none)
+ *   shared_gate_up [2Fs, d], shared_down [d, Fs]  act_dtype, NULL if shared_d_ff == 0
+ *   yperm          [N*k, d]       act_dtype  out: rows [0, num_kept) written
+ *   yshared        [N, d]         act_dtype  out: shared expert output (NULL if none)
+ * bf16: tensor-core products with fp32 accumulation; h is rounded to bf16.
+ * fp32: fp32 products and accumulation. */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* expert_start,
+                          const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
+                          const void* x, const void* shared_gate_up, const void* shared_down,
+                          void* yperm, void* yshared, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Combine.  Same page, step 4 (outputs return to token order, weighted by the router
+ * scores and summed); section "Load balancing and capacity" (a skipped token passes
+ * through the residual connection unchanged).
+ *   out[t] = residual[t] + yshared[t] + sum_{j kept} topk_w[t,j] * yperm[slot_of[t,j]]
+ * summed in fp32 in the order written (j ascending), rounded once to act_dtype.  A
+ * token with no kept choice and no shared expert gets out[t] == residual[t] exactly.
+ *   yperm [N*k, d], slot_of [N*k], topk_w [N, k], residual [N, d] or NULL,
+ *   yshared [N, d] or NULL, out [N, d]. */
+moe_status moe_combine(const moe_config* cfg, const void* yperm, const int32_t* slot_of,
+                       const float* topk_w, const void* residual, const void* yshared,
+                       void* out, void* stream);
+
+/* Bias-based balancing.  Same page, section "Load balancing and capacity": after a
+ * step, lower the selection bias of overloaded experts and raise it for underloaded
+ * ones.  For each expert e (fp32, in place):
+ *   sel_bias[e] -= step  if expert_counts[e] * E > N * k   (above the mean load)
+ *   sel_bias[e] += step  if expert_counts[e] * E < N * k
+ * equal load leaves it unchanged.  expert_counts [E] int32 (from moe_dispatch),
+ * sel_bias [E] fp32. */
+moe_status moe_bias_update(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
+                           float step, void* stream);
+
+/* Static, NUL-terminated description of a status code (host pointer). */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

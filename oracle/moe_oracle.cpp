@@ -1,0 +1,487 @@
+// moe_oracle.cpp -- plain, slow CPU oracle for the MoE layer hot path.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing on the product path may load, link or call
+// this file.  Only tests/, __graft_entry__.smoke() and the CPU-baseline leg of
+// bench.py use it, to check the CUDA library and to time a CPU baseline.  It
+// shares no code, header, table or constant generator with the CUDA sources.
+//
+// What it computes (the pages' MoE layer, one process, no device):
+//   1. router logits      logits[t,e] = sum_i x[t,i] W[e,i] + b[e]          (fp64 accumulate, one fp32 rounding)
+//   2. routing            score, optional group limit, top-k, combine weights
+//   3. counting           per-expert and per-rank assignment counts
+//   4. capacity           C = ceil(cf * N * k / E); overflow dropped in token order
+//   5. dispatch order     rank ascending, expert ascending, token order; slot_of / perm_src
+//   6. expert FFN         SwiGLU, fp64, no intermediate rounding
+//   7. combine            out[t] = x[t] + shared(x[t]) + sum_j w[t,j] y_j, fp64
+//   8. bias update        sign rule, fp32
+//
+// Sources ("the pages"):
+//   [UG] Ultralytics glossary "Expert Parallelism" (Chinese, German and Japanese
+//        editions carry the same text); sections "How tokens move between GPUs"
+//        (de: "Wie Tokens zwischen GPUs uebertragen werden") and "Load balancing
+//        and capacity" (de: "Lastausgleich und Kapazitaet").
+//   [BZ] bowenzhou.top knowledge planet, "专家并行" (expert parallelism); sections
+//        "机制：all-to-all 两轮" and the worked answer to exercise 2 (capacity factor).
+//   [FD] fudan-mlsys-cn chapter 10, section 10.5 (expert parallelism, shared experts).
+//
+// Readings where the pages are silent (each one is a choice, listed in the design notes):
+//   * ties in every ordering break toward the lower expert (or group) index;
+//   * softmax top-k selects on the logits themselves (softmax is monotone);
+//   * the sigmoid used for selection is the fp32 function S() below, fully specified
+//     from correctly rounded operations, so that two independent implementations
+//     reach identical selections;
+//   * group score = sum of the two largest selection scores in the group (the one
+//     largest if the group has a single expert);
+//   * capacity counts assignments, C = ceil(cf*N*k/E), drop priority is token order
+//     (then choice order j within a token), a dropped term is omitted with no
+//     re-normalisation of the remaining weights;
+//   * the layer output includes the residual, so a token whose every choice was
+//     dropped leaves the layer unchanged;
+//   * bias update compares the routed count with the mean load N*k/E.
+//
+// Build: g++ -O2 -fopenmp -ffp-contract=off -std=c++17 -shared -fPIC (see build.py).
+// -ffp-contract=off matters: the fp32 steps of S() must round exactly as written.
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+// ---------------------------------------------------------------- element access
+
+// bf16 is the upper half of an IEEE binary32; widening is exact.
+inline double bf16_bits_to_double(uint16_t v) {
+  uint32_t u = static_cast<uint32_t>(v) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return static_cast<double>(f);
+}
+
+// act_dtype: 0 = fp32, 1 = bf16 (stored as raw 16-bit patterns).
+inline double load_act(const void* base, int act_dtype, int64_t i) {
+  if (act_dtype == 0) return static_cast<double>(static_cast<const float*>(base)[i]);
+  return bf16_bits_to_double(static_cast<const uint16_t*>(base)[i]);
+}
+
+// ---------------------------------------------------------------- fp32 sigmoid spec
+//
+// S(l) = 1 / (1 + exp(-l)) evaluated in fp32 with a fixed sequence of correctly
+// rounded operations, so that any implementation that follows the same steps gets
+// the same bits:
+//   z  = clamp(-l, -20, 86)      (below -20 the fp32 result is exactly 1; above 86
+//                                 the result would leave the normal range)
+//   n  = rint(z * log2e)         fp32 multiply, round-half-even to integer
+//   r  = z - n*ln2_hi - n*ln2_lo two fused multiply-adds (Cody & Waite 1980 reduction:
+//                                 ln2_hi keeps 16 significant bits, ln2_lo the rest)
+//   p  = sum_{j=0..7} r^j / j!   degree-7 Taylor polynomial in Horner form, one fma
+//                                 per degree (|r| <= ln2/2, truncation < 4e-9 relative)
+//   e  = p * 2^n                 exact (power-of-two scale, n in [-29, 125])
+//   S  = 1 / (1 + e)             fp32 add, fp32 divide
+const float kLog2e = 0x1.715476p+0f;       // fp32 nearest to 1/ln 2
+const float kLn2Hi = 0x1.62e4p-1f;         // 45426 / 65536
+const float kLn2Lo = 0x1.7f7d1cp-20f;      // fp32 nearest to ln 2 - kLn2Hi
+const float kInvFact[8] = {1.0f, 1.0f, 0x1p-1f, 0x1.555556p-3f, 0x1.555556p-5f,
+                           0x1.111112p-7f, 0x1.6c16c2p-10f, 0x1.a01a02p-13f};
+
+float sigmoid_spec(float l) {
+  float z = -l;
+  z = std::fmax(z, -20.0f);
+  z = std::fmin(z, 86.0f);
+  float t = z * kLog2e;
+  float n = std::rint(t);
+  float r = std::fma(-n, kLn2Hi, z);
+  r = std::fma(-n, kLn2Lo, r);
+  float p = kInvFact[7];
+  for (int j = 6; j >= 0; --j) p = std::fma(p, r, kInvFact[j]);
+  int ni = static_cast<int>(n);
+  uint32_t sbits = static_cast<uint32_t>(ni + 127) << 23;
+  float scale;
+  std::memcpy(&scale, &sbits, 4);
+  float e = p * scale;
+  float den = 1.0f + e;
+  return 1.0f / den;
+}
+
+// ---------------------------------------------------------------- ordering
+
+struct Cand {
+  float key;
+  int idx;
+};
+// "a ranks before b": larger key first, lower index on equal keys.
+inline bool ranks_before(const Cand& a, const Cand& b) {
+  if (a.key != b.key) return a.key > b.key;
+  return a.idx < b.idx;
+}
+
+// Expert -> logical EP rank.  [UG] "How tokens move between GPUs": with E experts
+// on R devices, experts 0..E/R-1 live on device 0, the next E/R on device 1, and so
+// on (contiguous, rank = e / (E/R)).  Round-robin (rank = e mod R) is the decode
+// placement of the DeepSeek-V3-shaped workload.
+inline int rank_of(int e, int E, int R, int rank_map) {
+  if (rank_map == 1) return e % R;
+  return e / (E / R);
+}
+
+// SwiGLU expert FFN on one row, fp64 throughout.
+//   h_f = silu(x . Wgu[f]) * (x . Wgu[F + f]),  silu(z) = z / (1 + exp(-z))
+//   y_o = h . Wd[o]
+// Weight layout: Wgu [2F, d] (rows 0..F-1 gate, F..2F-1 up), Wd [d, F].
+// [UG] step 3: each device runs its local experts on the tokens it received; an
+// expert is a feed-forward block ([UG] intro); SwiGLU is the workloads' choice.
+void ffn_row(const double* x, int d, int F, int act_dtype, const void* wgu, int64_t wgu_off,
+             const void* wd, int64_t wd_off, double* y, std::vector<double>& h) {
+  h.assign(F, 0.0);
+  for (int f = 0; f < F; ++f) {
+    double g = 0.0, u = 0.0;
+    const int64_t rg = wgu_off + static_cast<int64_t>(f) * d;
+    const int64_t ru = wgu_off + static_cast<int64_t>(F + f) * d;
+    for (int i = 0; i < d; ++i) {
+      g += x[i] * load_act(wgu, act_dtype, rg + i);
+      u += x[i] * load_act(wgu, act_dtype, ru + i);
+    }
+    h[f] = g / (1.0 + std::exp(-g)) * u;
+  }
+  for (int o = 0; o < d; ++o) {
+    double acc = 0.0;
+    const int64_t ro = wd_off + static_cast<int64_t>(o) * F;
+    for (int f = 0; f < F; ++f) acc += h[f] * load_act(wd, act_dtype, ro + f);
+    y[o] = acc;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------- 0. helpers
+
+float oracle_sigmoid_spec(float l) { return sigmoid_spec(l); }
+
+void oracle_sigmoid_spec_many(int64_t n, const float* l, float* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = sigmoid_spec(l[i]);
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+int oracle_rank_of(int e, int E, int R, int rank_map) { return rank_of(e, E, R, rank_map); }
+
+// Capacity: [UG] "Load balancing and capacity": each expert takes at most a fixed
+// number per batch, e.g. 1.25 times its even share; [BZ] exercise 2: each expert's
+// buffer is reserved at the mean times 1.25.  The even share of N*k assignments over
+// E experts is N*k/E, so C = ceil(cf * N * k / E).  cf <= 0 means no cap (INT_MAX).
+int oracle_capacity(int N, int k, int E, float cf) {
+  if (!(cf > 0.0f)) return INT_MAX;
+  double c = std::ceil(static_cast<double>(cf) * static_cast<double>(N) * static_cast<double>(k) /
+                       static_cast<double>(E));
+  if (c > static_cast<double>(INT_MAX)) return INT_MAX;
+  return static_cast<int>(c);
+}
+
+// ---------------------------------------------------------------- 1. router logits
+//
+// [UG] step 1: the router scores every token against every expert; in the page's
+// example the router is a linear layer (hidden -> num_experts, with bias).
+// logits[t,e] = sum_i x[t,i] * W[e,i] + b[e], accumulated in fp64 and rounded once.
+// x: [N, d] in act_dtype; W: [E, d] fp32; b: [E] fp32 or null.
+int oracle_router_logits(int N, int d, int E, int act_dtype, const void* x, const float* W,
+                         const float* b, float* logits) {
+#pragma omp parallel
+  {
+    std::vector<double> xr(d);
+#pragma omp for schedule(static)
+    for (int t = 0; t < N; ++t) {
+      for (int i = 0; i < d; ++i) xr[i] = load_act(x, act_dtype, static_cast<int64_t>(t) * d + i);
+      for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        const float* w = W + static_cast<int64_t>(e) * d;
+        for (int i = 0; i < d; ++i) acc += xr[i] * static_cast<double>(w[i]);
+        if (b) acc += static_cast<double>(b[e]);
+        logits[static_cast<int64_t>(t) * E + e] = static_cast<float>(acc);
+      }
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------- 2. routing
+//
+// [UG] step 1: keep the k highest-scoring experts per token (k is typically 1, 2
+// or 8).  [UG] step 4: outputs are weighted by the router scores.
+// [UG] "Load balancing and capacity", bias-based balancing: a per-expert bias is
+// added to the router scores and affects only which experts are selected.
+// [UG] same section: each token is sent to experts on at most 4 of the 8 nodes
+// (group-limited routing; one group per node).
+//
+// score_fn 0 (softmax): selection key = logit; weight_j = softmax(logits)_j over all E
+//   experts, fp64; with normalize, weight_j / sum over the k selected.
+// score_fn 1 (sigmoid): s_e = S(l_e) (fp32 spec above); key_e = s_e + bias_e (one fp32
+//   add; bias may be null = 0); weight_j = s_j (no bias), with normalize divided by the
+//   sum of s over the k selected, fp64.
+// Group limit (num_groups > 1): groups are num_groups runs of E/num_groups contiguous
+//   experts; group score = fp32 sum of the two largest keys in the group; the
+//   topk_groups best groups (ties: lower group index) stay eligible.
+// Outputs: idx [N, k] int32 in selection order (best first); w64 [N, k] fp64.
+int oracle_route(int N, int E, int k, int score_fn, int normalize, int num_groups,
+                 int topk_groups, const float* logits, const float* sel_bias, int32_t* idx,
+                 double* w64) {
+  if (k < 1 || k > E) return -1;
+  if (num_groups < 1 || E % num_groups != 0) return -1;
+  if (topk_groups < 1 || topk_groups > num_groups) return -1;
+  const int gs = E / num_groups;
+  if (topk_groups * gs < k) return -1;
+#pragma omp parallel
+  {
+    std::vector<float> sig(E), key(E);
+    std::vector<Cand> cands, groups;
+    std::vector<char> allowed(E);
+#pragma omp for schedule(static)
+    for (int t = 0; t < N; ++t) {
+      const float* l = logits + static_cast<int64_t>(t) * E;
+      for (int e = 0; e < E; ++e) {
+        if (score_fn == 1) {
+          sig[e] = sigmoid_spec(l[e]);
+          key[e] = sel_bias ? sig[e] + sel_bias[e] : sig[e];
+        } else {
+          key[e] = l[e];
+        }
+        allowed[e] = 1;
+      }
+      if (num_groups > 1) {
+        groups.clear();
+        for (int g = 0; g < num_groups; ++g) {
+          std::vector<float> gk(key.begin() + g * gs, key.begin() + (g + 1) * gs);
+          std::sort(gk.begin(), gk.end(), [](float a, float b) { return a > b; });
+          float score = gs >= 2 ? gk[0] + gk[1] : gk[0];
+          groups.push_back({score, g});
+        }
+        std::sort(groups.begin(), groups.end(), ranks_before);
+        std::vector<char> gkeep(num_groups, 0);
+        for (int i = 0; i < topk_groups; ++i) gkeep[groups[i].idx] = 1;
+        for (int e = 0; e < E; ++e) allowed[e] = gkeep[e / gs];
+      }
+      cands.clear();
+      for (int e = 0; e < E; ++e)
+        if (allowed[e]) cands.push_back({key[e], e});
+      std::sort(cands.begin(), cands.end(), ranks_before);
+      int32_t* out_i = idx + static_cast<int64_t>(t) * k;
+      double* out_w = w64 + static_cast<int64_t>(t) * k;
+      for (int j = 0; j < k; ++j) out_i[j] = cands[j].idx;
+      if (score_fn == 1) {
+        double s = 0.0;
+        for (int j = 0; j < k; ++j) s += static_cast<double>(sig[out_i[j]]);
+        for (int j = 0; j < k; ++j) {
+          double v = static_cast<double>(sig[out_i[j]]);
+          out_w[j] = normalize ? v / s : v;
+        }
+      } else {
+        double m = -INFINITY;
+        for (int e = 0; e < E; ++e) m = std::max(m, static_cast<double>(l[e]));
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += std::exp(static_cast<double>(l[e]) - m);
+        double zs = 0.0;
+        for (int j = 0; j < k; ++j) zs += std::exp(static_cast<double>(l[out_i[j]]) - m);
+        for (int j = 0; j < k; ++j) {
+          double p = std::exp(static_cast<double>(l[out_i[j]]) - m);
+          out_w[j] = normalize ? p / zs : p / z;
+        }
+      }
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------- 3-5. count, cap, dispatch order
+//
+// [UG] "How tokens move between GPUs", step 2 and the example: count the
+// token-expert assignments per expert and per device (bincount of the chosen experts
+// and of their devices).  [UG] "Load balancing and capacity": over capacity, a token
+// skips that expert.  Dispatch (step 2) sends each token's hidden state to the device
+// holding its expert; the single-device equivalent is the permuted buffer an
+// all-to-all would send: rank-major, then expert, then token order.
+//
+// Inputs: idx [N, k].  Outputs:
+//   expert_counts [E]  routed assignments (before the cap)
+//   kept_counts   [E]  min(count, C)
+//   expert_start  [E]  first slot of each expert in the send buffer
+//   rank_counts   [R]  kept assignments per rank
+//   rank_offsets  [R+1] exclusive prefix of rank_counts
+//   slot_of       [N*k] slot of assignment a = t*k + j, or -1 if dropped
+//   perm_src      [N*k] perm_src[slot] = a for slot < num_kept, -1 beyond
+//   num_kept      [1]
+int oracle_dispatch(int N, int E, int k, int R, int rank_map, float cf, const int32_t* idx,
+                    int32_t* expert_counts, int32_t* kept_counts, int32_t* expert_start,
+                    int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
+                    int32_t* perm_src, int32_t* num_kept) {
+  if (R < 1 || R > E) return -1;
+  if (rank_map == 0 && E % R != 0) return -1;
+  const int64_t A = static_cast<int64_t>(N) * k;
+  const int C = oracle_capacity(N, k, E, cf);
+  std::vector<int64_t> seen(E, 0);
+  std::vector<int64_t> pos(A);
+  for (int e = 0; e < E; ++e) expert_counts[e] = 0;
+  for (int64_t a = 0; a < A; ++a) {  // token order: t major, choice j minor
+    const int e = idx[a];
+    if (e < 0 || e >= E) return -2;
+    pos[a] = seen[e]++;
+    expert_counts[e] += 1;
+  }
+  for (int e = 0; e < E; ++e) kept_counts[e] = std::min<int64_t>(expert_counts[e], C);
+  // send order: rank ascending, expert ascending inside a rank
+  std::vector<int> order(E);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    return rank_of(a, E, R, rank_map) < rank_of(b, E, R, rank_map);
+  });
+  int64_t run = 0;
+  for (int r = 0; r < R; ++r) rank_counts[r] = 0;
+  for (int i = 0; i < E; ++i) {
+    const int e = order[i];
+    expert_start[e] = static_cast<int32_t>(run);
+    run += kept_counts[e];
+    rank_counts[rank_of(e, E, R, rank_map)] += kept_counts[e];
+  }
+  rank_offsets[0] = 0;
+  for (int r = 0; r < R; ++r) rank_offsets[r + 1] = rank_offsets[r] + rank_counts[r];
+  *num_kept = static_cast<int32_t>(run);
+  for (int64_t a = 0; a < A; ++a) perm_src[a] = -1;
+  for (int64_t a = 0; a < A; ++a) {
+    const int e = idx[a];
+    if (pos[a] < C) {
+      const int64_t s = expert_start[e] + pos[a];
+      slot_of[a] = static_cast<int32_t>(s);
+      perm_src[s] = static_cast<int32_t>(a);
+    } else {
+      slot_of[a] = -1;
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------- 6. expert FFN
+//
+// y[i] = FFN_{expert[i]}(x[i]) for a list of rows (fp64 result).
+// xrows [n, d] act_dtype; expert ids [n] (an id equal to E selects the shared
+// expert, whose weights are passed separately); w_gate_up [E, 2F, d]; w_down [E, d, F];
+// shared weights [2Fs, d], [d, Fs] (null if Fs == 0).
+// [FD] 10.5: a shared expert processes every token and absorbs common patterns.
+int oracle_expert_rows(int n, int d, int E, int F, int Fs, int act_dtype, const void* xrows,
+                       const int32_t* expert, const void* w_gate_up, const void* w_down,
+                       const void* shared_gate_up, const void* shared_down, double* y) {
+#pragma omp parallel
+  {
+    std::vector<double> xr(d), h;
+#pragma omp for schedule(dynamic, 1)
+    for (int i = 0; i < n; ++i) {
+      for (int c = 0; c < d; ++c) xr[c] = load_act(xrows, act_dtype, static_cast<int64_t>(i) * d + c);
+      const int e = expert[i];
+      double* yr = y + static_cast<int64_t>(i) * d;
+      if (e == E) {
+        ffn_row(xr.data(), d, Fs, act_dtype, shared_gate_up, 0, shared_down, 0, yr, h);
+      } else {
+        ffn_row(xr.data(), d, F, act_dtype, w_gate_up, static_cast<int64_t>(e) * 2 * F * d, w_down,
+                static_cast<int64_t>(e) * d * F, yr, h);
+      }
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------- 7. combine
+//
+// [UG] step 4: expert outputs return to each token's home and are summed after
+// weighting by the router scores.  [UG] "Load balancing and capacity": a skipped
+// token passes through the layer unchanged via the residual connection.
+// out[t] = x[t] + ys[t] + sum_{j kept} w[t,j] * yperm[slot_of[t,j]], fp64, j ascending.
+// yperm: [*, d] in act_dtype (the values under test); ys: [N, d] act_dtype or null.
+// tokens: the list of token ids to produce (out is [ntok, d]).
+int oracle_combine(int ntok, const int32_t* tokens, int d, int k, int act_dtype, const void* x,
+                   const void* yperm, const void* ys, const int32_t* slot_of, const double* w,
+                   double* out) {
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < ntok; ++i) {
+    const int64_t t = tokens[i];
+    double* o = out + static_cast<int64_t>(i) * d;
+    for (int c = 0; c < d; ++c) {
+      double acc = load_act(x, act_dtype, t * d + c);
+      if (ys) acc += load_act(ys, act_dtype, t * d + c);
+      for (int j = 0; j < k; ++j) {
+        const int32_t s = slot_of[t * k + j];
+        if (s < 0) continue;
+        acc += w[t * k + j] * load_act(yperm, act_dtype, static_cast<int64_t>(s) * d + c);
+      }
+      o[c] = acc;
+    }
+  }
+  return 0;
+}
+
+// Whole layer for a list of tokens, from the hidden states and weights: the same
+// sum as oracle_combine, with every expert output computed here in fp64 (no
+// intermediate rounding).  Routing (idx, w, slot_of) is passed in.
+int oracle_layer_tokens(int ntok, const int32_t* tokens, int d, int E, int k, int F, int Fs,
+                        int act_dtype, const void* x, const int32_t* idx, const double* w,
+                        const int32_t* slot_of, const void* w_gate_up, const void* w_down,
+                        const void* shared_gate_up, const void* shared_down, double* out) {
+#pragma omp parallel
+  {
+    std::vector<double> xr(d), yr(d), h;
+#pragma omp for schedule(dynamic, 1)
+    for (int i = 0; i < ntok; ++i) {
+      const int64_t t = tokens[i];
+      for (int c = 0; c < d; ++c) xr[c] = load_act(x, act_dtype, t * d + c);
+      double* o = out + static_cast<int64_t>(i) * d;
+      for (int c = 0; c < d; ++c) o[c] = xr[c];
+      if (Fs > 0) {
+        ffn_row(xr.data(), d, Fs, act_dtype, shared_gate_up, 0, shared_down, 0, yr.data(), h);
+        for (int c = 0; c < d; ++c) o[c] += yr[c];
+      }
+      for (int j = 0; j < k; ++j) {
+        if (slot_of[t * k + j] < 0) continue;
+        const int e = idx[t * k + j];
+        ffn_row(xr.data(), d, F, act_dtype, w_gate_up, static_cast<int64_t>(e) * 2 * F * d, w_down,
+                static_cast<int64_t>(e) * d * F, yr.data(), h);
+        const double wj = w[t * k + j];
+        for (int c = 0; c < d; ++c) o[c] += wj * yr[c];
+      }
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------- 8. bias update
+//
+// [UG] "Load balancing and capacity", bias-based balancing: after each step the
+// bias of overloaded experts is lowered and the bias of underloaded experts raised.
+// Overloaded means more routed assignments than the mean load N*k/E (compared
+// exactly in integers as c*E vs N*k); equal load leaves the bias unchanged.
+// b_e <- b_e - step (fp32) if overloaded, b_e + step if underloaded.
+int oracle_bias_update(int E, int N, int k, const int32_t* counts, float step, float* bias) {
+  const int64_t mean_num = static_cast<int64_t>(N) * k;
+  for (int e = 0; e < E; ++e) {
+    const int64_t lhs = static_cast<int64_t>(counts[e]) * E;
+    if (lhs > mean_num) {
+      bias[e] = bias[e] - step;
+    } else if (lhs < mean_num) {
+      bias[e] = bias[e] + step;
+    }
+  }
+  return 0;
+}
+
+}  // extern "C"
