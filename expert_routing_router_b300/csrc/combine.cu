@@ -1,0 +1,147 @@
+// combine.cu -- weighted un-permute + sum (combine) and the bias update.
+//
+// Ultralytics glossary "Expert Parallelism", section "How tokens move between GPUs",
+// step 4: expert outputs return to each token's home, are weighted by the router
+// scores and summed.  Section "Load balancing and capacity": a token that skipped
+// its experts passes through the residual connection unchanged; after each step
+// the selection bias of overloaded experts is lowered and that of underloaded
+// experts raised.
+//
+// K5 gathers (rather than scatters) so that every output row is written exactly
+// once and the sum order is fixed: acc = residual; acc += yshared; acc += w_j*y_j
+// for j = 0..k-1 (kept choices only), fp32, one rounding to the output type.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int TC = 256;
+
+template <typename T>
+struct Vec;  // 16 bytes of T, widened to fp32
+template <>
+struct Vec<float> {
+  static constexpr int n = 4;
+  __device__ static void load(const void* p, float* f) {
+    const uint4 v = *static_cast<const uint4*>(p);
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ static void store(void* p, const float* f) {
+    *static_cast<uint4*>(p) =
+        make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                   __float_as_uint(f[3]));
+  }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int n = 8;
+  __device__ static void load(const void* p, float* f) {
+    const uint4 v = *static_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static void store(void* p, const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *static_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(TC)
+combine_kernel(const uint4* __restrict__ yperm, const int32_t* __restrict__ slot_of,
+               const float* __restrict__ topk_w, const uint4* __restrict__ residual,
+               const uint4* __restrict__ yshared, uint4* __restrict__ out, int N, int k, int nvec) {
+  constexpr int L = Vec<T>::n;
+  for (int t = blockIdx.x; t < N; t += gridDim.x) {
+    int slots[kMaxTopK];
+    float w[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      slots[j] = (j < k) ? slot_of[(int64_t)t * k + j] : -1;
+      w[j] = (j < k) ? topk_w[(int64_t)t * k + j] : 0.0f;
+    }
+    for (int v = threadIdx.x; v < nvec; v += TC) {
+      // issue every load of this vector position before any arithmetic
+      uint4 raw[kMaxTopK];
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (slots[j] >= 0) raw[j] = ld_stream_u4(yperm + (int64_t)slots[j] * nvec + v);
+      uint4 rres = make_uint4(0, 0, 0, 0), rsh = make_uint4(0, 0, 0, 0);
+      if (residual) rres = ld_stream_u4(residual + (int64_t)t * nvec + v);
+      if (yshared) rsh = ld_stream_u4(yshared + (int64_t)t * nvec + v);
+      float acc[L], tmp[L];
+      if (residual) {
+        Vec<T>::load(&rres, acc);
+      } else {
+#pragma unroll
+        for (int i = 0; i < L; ++i) acc[i] = 0.0f;
+      }
+      if (yshared) {
+        Vec<T>::load(&rsh, tmp);
+#pragma unroll
+        for (int i = 0; i < L; ++i) acc[i] += tmp[i];
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        if (slots[j] >= 0) {
+          Vec<T>::load(&raw[j], tmp);
+#pragma unroll
+          for (int i = 0; i < L; ++i) acc[i] = fmaf(w[j], tmp[i], acc[i]);
+        }
+      }
+      Vec<T>::store(out + (int64_t)t * nvec + v, acc);
+    }
+  }
+}
+
+__global__ void bias_update_kernel(const int32_t* __restrict__ counts, float* __restrict__ bias,
+                                   int E, int64_t mean_num, float step) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const int64_t lhs = (int64_t)counts[e] * E;
+  if (lhs > mean_num) {
+    bias[e] = __fsub_rn(bias[e], step);
+  } else if (lhs < mean_num) {
+    bias[e] = __fadd_rn(bias[e], step);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Cfg& c, const void* yperm, const int32_t* slot_of,
+                           const float* topk_w, const void* residual, const void* yshared,
+                           void* out, cudaStream_t s) {
+  const int nvec = (int)((int64_t)c.d * c.act_bytes / 16);
+  int grid = num_sms() * 8;
+  if (grid > c.N) grid = c.N;
+  const uint4* yp = static_cast<const uint4*>(yperm);
+  const uint4* rs = static_cast<const uint4*>(residual);
+  const uint4* ys = static_cast<const uint4*>(yshared);
+  uint4* o = static_cast<uint4*>(out);
+  if (c.act == MOE_DTYPE_F32)
+    combine_kernel<float><<<grid, TC, 0, s>>>(yp, slot_of, topk_w, rs, ys, o, c.N, c.k, nvec);
+  else
+    combine_kernel<__nv_bfloat16><<<grid, TC, 0, s>>>(yp, slot_of, topk_w, rs, ys, o, c.N, c.k,
+                                                       nvec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bias_update(const Cfg& c, const int32_t* expert_counts, float* sel_bias,
+                               float step, cudaStream_t s) {
+  bias_update_kernel<<<(c.E + 255) / 256, 256, 0, s>>>(expert_counts, sel_bias, c.E, c.A, step);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,218 @@
+// dispatch.cu -- counting, capacity, send-order slots, and the permute (dispatch).
+//
+// Ultralytics glossary "Expert Parallelism", section "How tokens move between GPUs",
+// step 2 and its example: count token-expert assignments per expert and per device,
+// and send each token's hidden state to the device holding its expert.  Section
+// "Load balancing and capacity": an expert accepts at most a fixed number of
+// tokens per batch (cf times its even share); the overflow skips that expert.
+//
+// Single-GPU form: the "send buffer" xperm holds the kept rows in the order an
+// all-to-all would send them (rank, then expert, then token order), and the
+// per-rank counts/offsets are its split sizes.  Deterministic, no inter-CTA waits:
+//   K2a count   one CTA per chunk of kChunk assignments: per-chunk histogram
+//   K2b scan    one CTA: per-expert prefix over chunks (chunk bases), routed counts,
+//               kept = min(count, C), send-order expert starts, rank counts/offsets
+//   K2c assign  one CTA per chunk: stable (token-order) rank of each assignment
+//               within its expert -> slot or drop; perm_src tail cleared
+//   K3  permute every token row read once, written to each of its kept slots
+//               (16-byte vector loads / stores)
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int T2 = 256;  // threads of the count / scan / assign kernels
+
+__global__ void __launch_bounds__(T2)
+count_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int32_t* __restrict__ chunk_hist) {
+  __shared__ int hist[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += T2) hist[e] = 0;
+  __syncthreads();
+  const int64_t a0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t a1 = min(a0 + kChunk, A);
+  for (int64_t a = a0 + threadIdx.x; a < a1; a += T2) {
+    const int e = idx[a];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += T2) chunk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Position of expert e in the send order (rank ascending, expert ascending).
+__device__ __forceinline__ int send_pos(int e, int E, int R, int rank_map) {
+  if (rank_map == MOE_RANK_ROUND_ROBIN) {
+    const int r = e % R, j = e / R;
+    const int q = E / R, rem = E % R;
+    return r * q + min(r, rem) + j;  // ranks below r hold q (+1 for the first rem) experts
+  }
+  return e;
+}
+
+__global__ void __launch_bounds__(T2)
+scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int R, int rank_map, int C,
+            int32_t* __restrict__ expert_counts, int32_t* __restrict__ kept_counts,
+            int32_t* __restrict__ expert_start, int32_t* __restrict__ rank_counts,
+            int32_t* __restrict__ rank_offsets, int32_t* __restrict__ num_kept) {
+  __shared__ int kept_by_pos[kMaxExperts];
+  __shared__ int start_by_pos[kMaxExperts + 1];
+  __shared__ int warp_tot[T2 / 32];
+  const int e = threadIdx.x;
+  int pos = 0, kept = 0;
+  if (e < E) {
+    int run = 0;
+    for (int c = 0; c < n_chunks; ++c) {  // coalesced across e
+      const int v = chunk_hist[(int64_t)c * E + e];
+      chunk_hist[(int64_t)c * E + e] = run;  // becomes the chunk's base for expert e
+      run += v;
+    }
+    kept = min(run, C);
+    expert_counts[e] = run;
+    kept_counts[e] = kept;
+    pos = send_pos(e, E, R, rank_map);
+    kept_by_pos[pos] = kept;
+  }
+  __syncthreads();
+  // exclusive scan of kept_by_pos over E <= 256 positions (thread i = position i)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int v = (threadIdx.x < E) ? kept_by_pos[threadIdx.x] : 0;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += warp_tot[w];
+  if (threadIdx.x < E) start_by_pos[threadIdx.x] = base + incl - v;
+  if (threadIdx.x == E - 1) start_by_pos[E] = base + incl;
+  __syncthreads();
+  if (e < E) expert_start[e] = start_by_pos[pos];
+  // ranks: send positions of rank r are [P_r, P_{r+1})
+  for (int r = threadIdx.x; r < R; r += T2) {
+    int p0, p1;
+    if (rank_map == MOE_RANK_ROUND_ROBIN) {
+      const int q = E / R, rem = E % R;
+      p0 = r * q + min(r, rem);
+      p1 = p0 + q + (r < rem ? 1 : 0);
+    } else {
+      p0 = r * (E / R);
+      p1 = p0 + E / R;
+    }
+    rank_offsets[r] = start_by_pos[p0];
+    rank_counts[r] = start_by_pos[p1] - start_by_pos[p0];
+    if (r == R - 1) rank_offsets[R] = start_by_pos[p1];
+  }
+  if (threadIdx.x == 0) *num_kept = start_by_pos[E];
+}
+
+__global__ void __launch_bounds__(T2)
+assign_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int C,
+              const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ expert_start,
+              const int32_t* __restrict__ num_kept, int32_t* __restrict__ slot_of,
+              int32_t* __restrict__ perm_src) {
+  __shared__ int run[kMaxExperts];
+  __shared__ int wcnt[T2 / 32][kMaxExperts];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t a0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t a1 = min(a0 + kChunk, A);
+  for (int e = tid; e < E; e += T2) run[e] = chunk_base[(int64_t)blockIdx.x * E + e];
+  for (int64_t a = a0; a < a1; a += T2) {
+    for (int q = tid; q < (T2 / 32) * E; q += T2) wcnt[q / E][q % E] = 0;
+    __syncthreads();  // also orders run[] updates of the previous round
+    const int64_t my = a + tid;
+    int e = -1;
+    if (my < a1) {
+      e = idx[my];
+      if ((unsigned)e >= (unsigned)E) e = -1;
+    }
+    const int key = (e >= 0) ? e : -1 - lane;  // invalid lanes never group together
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const int rank_in_warp = __popc(peers & lanemask_lt());
+    if (e >= 0 && rank_in_warp == 0) wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    int pos = 0;
+    if (e >= 0) {
+      pos = run[e] + rank_in_warp;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w][e];
+    }
+    __syncthreads();
+    for (int q = tid; q < E; q += T2) {
+      int s = 0;
+      for (int w = 0; w < T2 / 32; ++w) s += wcnt[w][q];
+      run[q] += s;
+    }
+    if (my < a1) {
+      if (e >= 0 && pos < C) {
+        const int slot = expert_start[e] + pos;
+        slot_of[my] = slot;
+        perm_src[slot] = (int32_t)my;
+      } else {
+        slot_of[my] = -1;
+      }
+    }
+    __syncthreads();  // wcnt is cleared at the top of the next round
+  }
+  // rows past num_kept carry no assignment
+  const int nk = *num_kept;
+  for (int64_t s = a0 + tid; s < a1; s += T2)
+    if (s >= nk) perm_src[s] = -1;
+}
+
+// K3: one CTA walks tokens; each 16-byte vector of a row is loaded once and stored
+// to every kept slot of that token.
+constexpr int TP = 256;
+constexpr int UNROLL = 4;
+
+__global__ void __launch_bounds__(TP)
+permute_kernel(const uint4* __restrict__ x, uint4* __restrict__ xperm,
+               const int32_t* __restrict__ slot_of, int N, int k, int nvec) {
+  for (int t = blockIdx.x; t < N; t += gridDim.x) {
+    int slots[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) slots[j] = (j < k) ? slot_of[(int64_t)t * k + j] : -1;
+    const uint4* src = x + (int64_t)t * nvec;
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += TP * UNROLL) {
+      uint4 buf[UNROLL];
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int v = v0 + u * TP;
+        if (v < nvec) buf[u] = ld_stream_u4(src + v);
+      }
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int v = v0 + u * TP;
+        if (v < nvec) {
+#pragma unroll
+          for (int j = 0; j < kMaxTopK; ++j)
+            if (slots[j] >= 0) xperm[(int64_t)slots[j] * nvec + v] = buf[u];
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Cfg& c, const int32_t* topk_idx, const void* x, void* xperm,
+                            int32_t* expert_counts, int32_t* kept_counts, int32_t* expert_start,
+                            int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
+                            int32_t* perm_src, int32_t* num_kept, int32_t* chunk_hist,
+                            cudaStream_t s) {
+  count_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.E, chunk_hist);
+  scan_kernel<<<1, T2, 0, s>>>(chunk_hist, c.n_chunks, c.E, c.R, c.rank_map, c.C, expert_counts,
+                               kept_counts, expert_start, rank_counts, rank_offsets, num_kept);
+  assign_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.E, c.C, chunk_hist, expert_start,
+                                          num_kept, slot_of, perm_src);
+  if (xperm) {
+    const int nvec = (int)((int64_t)c.d * c.act_bytes / 16);
+    int grid = num_sms() * 8;
+    if (grid > c.N) grid = c.N;
+    permute_kernel<<<grid, TP, 0, s>>>(static_cast<const uint4*>(x), static_cast<uint4*>(xperm),
+                                       slot_of, c.N, c.k, nvec);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,86 @@
+// moe_internal.cuh -- shared pieces of the CUDA library (never seen by callers).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kMaxGroups = 32;
+constexpr int kChunk = 2048;  // assignments per dispatch chunk (counting / slot pass)
+
+// ---------------------------------------------------------------- host-side view
+struct Cfg {
+  int N, d, E, k, R, rank_map, score_fn, normalize, G, TG, F, Fs, act;
+  float cf;
+  int64_t A;       // N * k assignments
+  int C;           // capacity (INT32 max = none)
+  int n_chunks;    // ceil(A / kChunk)
+  int act_bytes;   // 4 (fp32) or 2 (bf16)
+};
+
+// Workspace carve-up (one layout serves every call).
+struct WsLayout {
+  size_t chunk_hist;  // [n_chunks, E] int32
+  size_t h;           // FFN intermediate: [A, F] then [N, Fs], act dtype
+  size_t sched;       // tile scheduler scratch
+  size_t total;
+};
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// 16-byte read-only streaming load (data read once in the kernel).
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+}  // namespace moe
+
+// ---------------------------------------------------------------- launchers (host)
+namespace moe {
+cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, const float* b_router,
+                         const float* sel_bias, float* logits, int32_t* topk_idx, float* topk_w,
+                         cudaStream_t s);
+cudaError_t launch_dispatch(const Cfg& c, const int32_t* topk_idx, const void* x, void* xperm,
+                            int32_t* expert_counts, int32_t* kept_counts, int32_t* expert_start,
+                            int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
+                            int32_t* perm_src, int32_t* num_kept, int32_t* chunk_hist,
+                            cudaStream_t s);
+cudaError_t launch_ffn_simt(const Cfg& c, const void* xperm, const int32_t* expert_start,
+                            const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
+                            const void* x, const void* shared_gate_up, const void* shared_down,
+                            void* yperm, void* yshared, void* h, cudaStream_t s);
+cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert_start,
+                          const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
+                          const void* x, const void* shared_gate_up, const void* shared_down,
+                          void* yperm, void* yshared, void* h, void* sched, cudaStream_t s);
+cudaError_t launch_combine(const Cfg& c, const void* yperm, const int32_t* slot_of,
+                           const float* topk_w, const void* residual, const void* yshared,
+                           void* out, cudaStream_t s);
+cudaError_t launch_bias_update(const Cfg& c, const int32_t* expert_counts, float* sel_bias,
+                               float step, cudaStream_t s);
+int num_sms();
+}  // namespace moe

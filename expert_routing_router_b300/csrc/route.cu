@@ -1,0 +1,304 @@
+// route.cu -- router scoring + top-k selection (one fused kernel).
+//
+// Ultralytics glossary "Expert Parallelism", section "How tokens move between GPUs",
+// step 1: the router (a linear layer hidden -> num_experts) scores every token
+// against every expert and keeps the k best; step 4: the outputs are later weighted
+// by the router scores.  Section "Load balancing and capacity": DeepSeek-V3 adds a
+// per-expert bias to the scores that only changes which experts are selected, and
+// lets a token reach experts on at most 4 of 8 nodes (group-limited routing).
+//
+// One CTA owns 32 tokens and all E <= 256 experts, so the whole logits row of a
+// token is on chip when its selection runs:
+//   phase 1  logits tile [32, E] = x[32, d] . W[E, d]^T in fp32 FMAs (SIMT), d in
+//            chunks of 32 staged through shared memory;
+//   phase 2  + router bias, logits written out, then one warp per token: score,
+//            optional group limit, k rounds of warp-shuffle arg-max, weights.
+// Ordering everywhere: larger key first, lower expert (group) index on ties.
+#include <float.h>
+#include <math.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int TM = 32;        // tokens per CTA
+constexpr int KC = 32;        // d-chunk
+constexpr int THREADS = 256;  // 8 warps
+constexpr int MAXJ = kMaxExperts / 32;
+
+// fp32 sigmoid, evaluated as a fixed sequence of correctly rounded operations:
+// clamp -l to [-20, 86]; n = rint(z*log2e); Cody & Waite (1980) reduction
+// r = z - n*ln2_hi - n*ln2_lo with ln2_hi = 45426/65536; p = degree-7 Taylor
+// polynomial of e^r in Horner form (one fused multiply-add per degree, coefficients
+// 1/j! rounded to fp32); e = p * 2^n; S = 1 / (1 + e).  Any implementation of these
+// steps returns the same bits, so selection on S + bias is reproducible off-device.
+__device__ __forceinline__ float sigmoid_fixed(float l) {
+  const float z = fminf(fmaxf(-l, -20.0f), 86.0f);
+  const float n = rintf(__fmul_rn(z, 0x1.715476p+0f));
+  float r = __fmaf_rn(-n, 0x1.62e4p-1f, z);
+  r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
+  float p = 0x1.a01a02p-13f;         // 1/7!
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/6!
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/5!
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/4!
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/3!
+  p = __fmaf_rn(p, r, 0x1p-1f);          // 1/2!
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const float two_n = __int_as_float((__float2int_rn(n) + 127) << 23);
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, __fmul_rn(p, two_n)));
+}
+
+struct Best {
+  float key;
+  int idx;
+  float val;
+};
+
+// a ranks before b: larger key, or equal key and lower index.
+__device__ __forceinline__ bool before(float ka, int ia, float kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
+
+__device__ __forceinline__ Best warp_best(Best b) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float k2 = __shfl_xor_sync(0xffffffffu, b.key, off);
+    const int i2 = __shfl_xor_sync(0xffffffffu, b.idx, off);
+    const float v2 = __shfl_xor_sync(0xffffffffu, b.val, off);
+    if (before(k2, i2, b.key, b.idx)) {
+      b.key = k2;
+      b.idx = i2;
+      b.val = v2;
+    }
+  }
+  return b;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+struct RouteParams {
+  int N, d, E, k, score_fn, normalize, G, TG;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(THREADS)
+route_kernel(const T* __restrict__ x, const float* __restrict__ W, const float* __restrict__ b,
+             const float* __restrict__ sel_bias, float* __restrict__ logits,
+             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteParams p) {
+  extern __shared__ float smem[];
+  const int E = p.E;
+  const int EP = E + 1;                       // padded row of the logits tile
+  float* xs = smem;                           // [TM][KC + 1]
+  float* ws = smem + TM * (KC + 1);           // [E][KC + 1]
+  float* lt = smem;                           // phase 2: [TM][E + 1] (reuses phase-1 space)
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int t0 = blockIdx.x * TM;
+  const int EJ = (E + 31) / 32;
+
+  // ---------------- phase 1: logits tile
+  float acc[4][MAXJ];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) acc[i][j] = 0.0f;
+
+  for (int k0 = 0; k0 < p.d; k0 += KC) {
+    __syncthreads();
+    for (int q = tid; q < TM * KC; q += THREADS) {
+      const int r = q / KC, c = q % KC;
+      const int t = t0 + r, kk = k0 + c;
+      xs[r * (KC + 1) + c] = (t < p.N && kk < p.d) ? to_f32(x[(int64_t)t * p.d + kk]) : 0.0f;
+    }
+    for (int q = tid; q < E * KC; q += THREADS) {
+      const int e = q / KC, c = q % KC;
+      const int kk = k0 + c;
+      ws[e * (KC + 1) + c] = (kk < p.d) ? W[(int64_t)e * p.d + kk] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < KC; ++c) {
+      float xv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xv[i] = xs[(warp * 4 + i) * (KC + 1) + c];
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j) {
+        if (j < EJ) {
+          const int e = lane + 32 * j;
+          const float wv = (e < E) ? ws[e * (KC + 1) + c] : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i][j] = fmaf(xv[i], wv, acc[i][j]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---------------- phase 2a: bias, logits out
+#pragma unroll
+  for (int j = 0; j < MAXJ; ++j) {
+    const int e = lane + 32 * j;
+    if (j < EJ && e < E) {
+      const float be = b ? b[e] : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lt[(warp * 4 + i) * EP + e] = acc[i][j] + be;
+    }
+  }
+  __syncthreads();
+  for (int q = tid; q < TM * E; q += THREADS) {
+    const int r = q / E, e = q % E;
+    const int t = t0 + r;
+    if (t < p.N) logits[(int64_t)t * E + e] = lt[r * EP + e];
+  }
+  __syncthreads();  // rows are overwritten with ranking keys below
+
+  // ---------------- phase 2b: selection, one warp per token
+  const int gs = E / p.G;
+  for (int r = warp; r < TM; r += THREADS / 32) {
+    const int t = t0 + r;
+    if (t >= p.N) break;
+    float* row = lt + r * EP;
+    float key[MAXJ], val[MAXJ];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) {
+      const int e = lane + 32 * j;
+      key[j] = -INFINITY;
+      val[j] = 0.0f;
+      if (j < EJ && e < E) {
+        const float l = row[e];
+        if (p.score_fn == MOE_SCORE_SIGMOID) {
+          const float s = sigmoid_fixed(l);
+          val[j] = s;
+          key[j] = sel_bias ? __fadd_rn(s, sel_bias[e]) : s;
+        } else {
+          val[j] = l;
+          key[j] = l;
+        }
+        valid |= 1u << j;
+      }
+    }
+    if (p.G > 1) {
+      // ranking keys into the row (the warp owns it), then lane g < G scans group g
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j) {
+        const int e = lane + 32 * j;
+        if (j < EJ && e < E) row[e] = key[j];
+      }
+      __syncwarp();
+      float gscore = -INFINITY;
+      int gid = INT_MAX;
+      if (lane < p.G) {
+        float a = -INFINITY, c = -INFINITY;  // largest, second largest
+        for (int i = 0; i < gs; ++i) {
+          const float v = row[lane * gs + i];
+          if (v > a) {
+            c = a;
+            a = v;
+          } else if (v > c) {
+            c = v;
+          }
+        }
+        gscore = (gs >= 2) ? __fadd_rn(a, c) : a;
+        gid = lane;
+      }
+      uint32_t gmask = 0;
+      for (int it = 0; it < p.TG; ++it) {
+        Best bb = warp_best(Best{gscore, gid, 0.0f});
+        gmask |= 1u << bb.idx;
+        if (gid == bb.idx) {
+          gscore = -INFINITY;
+          gid = INT_MAX;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j) {
+        const int e = lane + 32 * j;
+        if ((valid >> j & 1u) && !((gmask >> (e / gs)) & 1u)) valid &= ~(1u << j);
+      }
+    }
+    // k rounds of arg-max
+    int sel_idx = -1;
+    float sel_val = 0.0f;
+    for (int it = 0; it < p.k; ++it) {
+      Best mine{-INFINITY, INT_MAX, 0.0f};
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j) {
+        if ((valid >> j) & 1u) {
+          const int e = lane + 32 * j;
+          if (before(key[j], e, mine.key, mine.idx)) mine = Best{key[j], e, val[j]};
+        }
+      }
+      const Best bb = warp_best(mine);
+      if (bb.idx < E && (bb.idx & 31) == lane) valid &= ~(1u << (bb.idx >> 5));
+      if (lane == it) {
+        sel_idx = bb.idx;
+        sel_val = bb.val;
+      }
+    }
+    // weights
+    float w;
+    if (p.score_fn == MOE_SCORE_SIGMOID) {
+      const float ssum = warp_sum(lane < p.k ? sel_val : 0.0f);
+      w = p.normalize ? sel_val / ssum : sel_val;
+    } else {
+      float m = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j)
+        if (j < EJ && lane + 32 * j < E) m = fmaxf(m, val[j]);
+      m = warp_max(m);
+      float z = 0.0f;
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j)
+        if (j < EJ && lane + 32 * j < E) z += expf(val[j] - m);
+      z = warp_sum(z);
+      const float pe = (lane < p.k) ? expf(sel_val - m) : 0.0f;
+      const float zsel = warp_sum(pe);
+      w = p.normalize ? pe / zsel : pe / z;
+    }
+    if (lane < p.k) {
+      topk_idx[(int64_t)t * p.k + lane] = sel_idx;
+      topk_w[(int64_t)t * p.k + lane] = w;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, const float* b_router,
+                         const float* sel_bias, float* logits, int32_t* topk_idx, float* topk_w,
+                         cudaStream_t s) {
+  RouteParams p{c.N, c.d, c.E, c.k, c.score_fn, c.normalize, c.G, c.TG};
+  const size_t sm1 = (size_t)(TM * (KC + 1) + c.E * (KC + 1)) * sizeof(float);
+  const size_t sm2 = (size_t)TM * (c.E + 1) * sizeof(float);
+  const size_t smem = sm1 > sm2 ? sm1 : sm2;
+  const dim3 grid((c.N + TM - 1) / TM);
+  if (c.act == MOE_DTYPE_F32) {
+    auto kern = route_kernel<float>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<grid, THREADS, smem, s>>>(static_cast<const float*>(x), w_router, b_router, sel_bias,
+                                     logits, topk_idx, topk_w, p);
+  } else {
+    auto kern = route_kernel<__nv_bfloat16>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<grid, THREADS, smem, s>>>(static_cast<const __nv_bfloat16*>(x), w_router, b_router,
+                                     sel_bias, logits, topk_idx, topk_w, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,180 @@
+"""ctypes binding of libmoe.so -- argument marshalling only.
+
+Every function below has the name of the C entry point it calls (include/moe.h)
+and forwards torch tensors as raw device pointers.  No step of the layer runs in
+Python: if the library is missing the import-time loader raises, and there is no
+fallback of any kind.  Tensors must already be on the GPU with the layouts the
+header documents.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = range(5)
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("num_ranks", ctypes.c_int32), ("rank_map", ctypes.c_int32),
+                ("score_fn", ctypes.c_int32), ("normalize_topk", ctypes.c_int32),
+                ("num_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float), ("d_ff", ctypes.c_int32),
+                ("shared_d_ff", ctypes.c_int32), ("act_dtype", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)}")
+
+
+EXPORTS = ("moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+           "moe_bias_update", "moe_status_string")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run "
+                          "`python expert_routing_router_b300/build.py`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, S, I, F = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+    C = ctypes.POINTER(moe_config)
+    lib.moe_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_route.argtypes = [C] + [P] * 8 + [S, P]
+    lib.moe_dispatch.argtypes = [C] + [P] * 12 + [S, P]
+    lib.moe_expert_ffn.argtypes = [C] + [P] * 11 + [S, P]
+    lib.moe_combine.argtypes = [C] + [P] * 6 + [P]
+    lib.moe_bias_update.argtypes = [C, P, P, F, P]
+    lib.moe_status_string.argtypes = [I]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    for fn in EXPORTS[:-1]:
+        getattr(lib, fn).restype = I
+    return lib
+
+
+_lib = _load()
+lib = _lib
+
+
+def status_string(status):
+    return _lib.moe_status_string(int(status)).decode()
+
+
+def config(w):
+    """moe_config for a workloads.Workload (or any object with the same fields)."""
+    return moe_config(w.tokens, w.hidden, w.num_experts, w.top_k, w.num_ranks, w.rank_map,
+                      w.score_fn, int(bool(w.normalize_topk)), w.num_groups, w.topk_groups,
+                      float(w.capacity_factor), w.d_ff, w.shared_d_ff,
+                      DTYPE_F32 if w.act_dtype == "f32" else DTYPE_BF16)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, status):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def moe_workspace_size(cfg):
+    n = ctypes.c_size_t(0)
+    _check("moe_workspace_size", _lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def moe_route(cfg, x, w_router, b_router, sel_bias, logits, topk_idx, topk_w, workspace,
+              stream=None):
+    _check("moe_route", _lib.moe_route(
+        ctypes.byref(cfg), _p(x), _p(w_router), _p(b_router), _p(sel_bias), _p(logits),
+        _p(topk_idx), _p(topk_w), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_dispatch(cfg, topk_idx, x, xperm, expert_counts, kept_counts, expert_start, rank_counts,
+                 rank_offsets, slot_of, perm_src, num_kept, workspace, stream=None):
+    _check("moe_dispatch", _lib.moe_dispatch(
+        ctypes.byref(cfg), _p(topk_idx), _p(x), _p(xperm), _p(expert_counts), _p(kept_counts),
+        _p(expert_start), _p(rank_counts), _p(rank_offsets), _p(slot_of), _p(perm_src),
+        _p(num_kept), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_expert_ffn(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x, shared_gate_up,
+                   shared_down, yperm, yshared, workspace, stream=None):
+    _check("moe_expert_ffn", _lib.moe_expert_ffn(
+        ctypes.byref(cfg), _p(xperm), _p(expert_start), _p(kept_counts), _p(w_gate_up),
+        _p(w_down), _p(x), _p(shared_gate_up), _p(shared_down), _p(yperm), _p(yshared),
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_combine(cfg, yperm, slot_of, topk_w, residual, yshared, out, stream=None):
+    _check("moe_combine", _lib.moe_combine(
+        ctypes.byref(cfg), _p(yperm), _p(slot_of), _p(topk_w), _p(residual), _p(yshared),
+        _p(out), _stream(stream)))
+
+
+def moe_bias_update(cfg, expert_counts, sel_bias, step, stream=None):
+    _check("moe_bias_update", _lib.moe_bias_update(
+        ctypes.byref(cfg), _p(expert_counts), _p(sel_bias), float(step), _stream(stream)))
+
+
+class LayerBuffers:
+    """Device buffers of one layer call, sized for the worst case (N*k kept rows)."""
+
+    def __init__(self, w, device="cuda"):
+        N, d, E, k, R = w.tokens, w.hidden, w.num_experts, w.top_k, w.num_ranks
+        dt = w.torch_dtype
+        i32 = dict(dtype=torch.int32, device=device)
+        self.cfg = config(w)
+        self.logits = torch.empty(N, E, dtype=torch.float32, device=device)
+        self.topk_idx = torch.empty(N, k, **i32)
+        self.topk_w = torch.empty(N, k, dtype=torch.float32, device=device)
+        self.xperm = torch.empty(N * k, d, dtype=dt, device=device)
+        self.yperm = torch.empty(N * k, d, dtype=dt, device=device)
+        self.yshared = torch.empty(N, d, dtype=dt, device=device) if w.shared_d_ff else None
+        self.out = torch.empty(N, d, dtype=dt, device=device)
+        self.expert_counts = torch.empty(E, **i32)
+        self.kept_counts = torch.empty(E, **i32)
+        self.expert_start = torch.empty(E, **i32)
+        self.rank_counts = torch.empty(R, **i32)
+        self.rank_offsets = torch.empty(R + 1, **i32)
+        self.slot_of = torch.empty(N * k, **i32)
+        self.perm_src = torch.empty(N * k, **i32)
+        self.num_kept = torch.empty(1, **i32)
+        nbytes = moe_workspace_size(self.cfg)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def run_layer(b, inp, bias_step=0.0, stream=None):
+    """One pass of the layer path through the C ABI: route, dispatch, expert FFN,
+    combine, and (if bias_step) the selection-bias update."""
+    c = b.cfg
+    moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"], b.logits,
+              b.topk_idx, b.topk_w, b.workspace, stream)
+    moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
+                 b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
+                 b.num_kept, b.workspace, stream)
+    moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"], inp["w_down"],
+                   inp["x"], inp["shared_gate_up"], inp["shared_down"], b.yperm, b.yshared,
+                   b.workspace, stream)
+    moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out, stream)
+    if bias_step and inp["sel_bias"] is not None:
+        moe_bias_update(c, b.expert_counts, inp["sel_bias"], bias_step, stream)
+    return b.out

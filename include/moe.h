@@ -39,6 +39,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -87,7 +93,7 @@ typedef struct {
  * device memory, 256-byte aligned, owned by the caller; its contents on entry do not
  * matter and on exit are unspecified.  Calls sharing one workspace must not overlap
  * on the GPU. */
-moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Routing.  Ultralytics glossary "Expert Parallelism", section "How tokens move
  * between GPUs", step 1 (the router scores each token against every expert and keeps
@@ -108,7 +114,7 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
  * k kept if normalize_topk.  Group limit: group score = sum of the two best ranking
  * keys in the group; only the topk_groups best groups are eligible.  Ties break
  * toward the lower expert / group index. */
-moe_status moe_route(const moe_config* cfg, const void* x, const float* w_router,
+MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* w_router,
                      const float* b_router, const float* sel_bias, float* logits,
                      int32_t* topk_idx, float* topk_w, void* workspace,
                      size_t workspace_bytes, void* stream);
@@ -133,7 +139,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* w_router
  *                                       (s < num_kept), -1 for s >= num_kept
  *   num_kept      [1]        int32      out: rows written to xperm
  * xperm may be NULL to compute the routing tables only (x is then ignored). */
-moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
                         void* xperm, int32_t* expert_counts, int32_t* kept_counts,
                         int32_t* expert_start, int32_t* rank_counts, int32_t* rank_offsets,
                         int32_t* slot_of, int32_t* perm_src, int32_t* num_kept,
@@ -154,7 +160,7 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const vo
  *   yshared        [N, d]         act_dtype  out: shared expert output (NULL if none)
  * bf16: tensor-core products with fp32 accumulation; h is rounded to bf16.
  * fp32: fp32 products and accumulation. */
-moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* expert_start,
+MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* expert_start,
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,
                           void* yperm, void* yshared, void* workspace, size_t workspace_bytes,
@@ -168,7 +174,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_
  * token with no kept choice and no shared expert gets out[t] == residual[t] exactly.
  *   yperm [N*k, d], slot_of [N*k], topk_w [N, k], residual [N, d] or NULL,
  *   yshared [N, d] or NULL, out [N, d]. */
-moe_status moe_combine(const moe_config* cfg, const void* yperm, const int32_t* slot_of,
+MOE_API moe_status moe_combine(const moe_config* cfg, const void* yperm, const int32_t* slot_of,
                        const float* topk_w, const void* residual, const void* yshared,
                        void* out, void* stream);
 
@@ -179,11 +185,11 @@ moe_status moe_combine(const moe_config* cfg, const void* yperm, const int32_t* 
  *   sel_bias[e] += step  if expert_counts[e] * E < N * k
  * equal load leaves it unchanged.  expert_counts [E] int32 (from moe_dispatch),
  * sel_bias [E] fp32. */
-moe_status moe_bias_update(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
+MOE_API moe_status moe_bias_update(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
                            float step, void* stream);
 
 /* Static, NUL-terminated description of a status code (host pointer). */
-const char* moe_status_string(moe_status status);
+MOE_API const char* moe_status_string(moe_status status);
 
 #ifdef __cplusplus
 }

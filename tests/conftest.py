@@ -30,3 +30,14 @@ def read_golden(name):
 @pytest.fixture(scope="session")
 def golden():
     return read_golden
+
+
+@pytest.fixture(scope="session")
+def moe_lib():
+    """The CUDA library's binding; builds libmoe.so in-tree first if it is missing."""
+    from expert_routing_router_b300 import build as _b
+    lib_path = os.path.join(ROOT, "expert_routing_router_b300", "libmoe.so")
+    if not os.path.exists(lib_path):
+        _b.build()
+    from expert_routing_router_b300 import moe
+    return moe

@@ -1,0 +1,261 @@
+"""GPU parity: every step of the CUDA path against the CPU oracle (needs a B300).
+
+Per step, the oracle gets the very inputs the GPU step got, so each comparison
+isolates one kernel:
+  logits            oracle fp64 logits of the same x, W, b          max-abs rel 1e-5
+  routing           oracle routing of the GPU's own logits          bit-exact indices,
+                                                                    weights rel 1e-5
+  dispatch tables   oracle dispatch of the GPU's own top-k ids      bit-exact
+  send buffer       xperm[s] == x[perm_src[s] // k]                 bit-exact
+  expert FFN        oracle fp64 FFN of the GPU's xperm rows         1e-4 (fp32) / 2e-2 (bf16)
+  combine           oracle fp64 sum of the GPU's yperm / weights    one output rounding
+  layer             oracle fp64 layer from x and the weights        1e-4 (fp32) / 2e-2 (bf16)
+  bias update       oracle fp32 sign rule                           bit-exact
+Tolerances are max-abs normalised: max|got - ref| <= tol * max|ref|.  Full-size
+workloads are checked on seeded samples of rows / tokens (always including every
+token whose choices were all dropped, up to a bound); the small cases are checked
+in full.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from expert_routing_router_b300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_LOGITS = 1e-5
+TOL_W = 1e-5
+TOL_OUT = {"f32": 1e-4, "bf16": 2e-2}
+TOL_COMBINE = {"f32": 2e-6, "bf16": 4e-3}
+
+
+def host(t):
+    """Tensor -> numpy: fp32 as float32, bf16 as uint16 bit patterns."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def f64(t):
+    return t.detach().cpu().double().numpy()
+
+
+def close(got, ref, tol, what):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.max(np.abs(got - ref)) if got.size else 0.0
+    scale = np.max(np.abs(ref)) if ref.size else 0.0
+    assert err <= tol * scale, f"{what}: max|err| {err:.3e} > {tol} * max|ref| {scale:.3e}"
+    return err / scale if scale else 0.0
+
+
+def run_gpu(w, inp):
+    from expert_routing_router_b300 import moe
+    b = moe.LayerBuffers(w)
+    bias_before = None if inp["sel_bias"] is None else inp["sel_bias"].clone()
+    moe.run_layer(b, inp)
+    torch.cuda.synchronize()
+    return b, bias_before
+
+
+def host_weights(inp):
+    """Host copies of the expert weights (made once per input set)."""
+    return {k: None if inp[k] is None else host(inp[k])
+            for k in ("w_gate_up", "w_down", "shared_gate_up", "shared_down")}
+
+
+def check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=None):
+    """All per-step and end-to-end checks for one layer call."""
+    if hw is None:
+        hw = host_weights(inp)
+    rng = np.random.default_rng(seed)
+    N, k, E = w.tokens, w.top_k, w.num_experts
+    x_h = host(inp["x"])
+    # ---- logits (sampled rows at full size)
+    rows = np.arange(N) if n_sample_tokens is None else np.sort(
+        rng.choice(N, size=min(N, 4 * n_sample_tokens), replace=False))
+    ref_l = oracle.router_logits(x_h[rows], host(inp["w_router"]), host(inp["b_router"]))
+    got_l = host(b.logits)
+    close(got_l[rows], ref_l, TOL_LOGITS, "router logits")
+    # ---- routing from the GPU's own logits: bit-exact ids
+    sb = None if inp["sel_bias"] is None else host(inp["sel_bias"])
+    idx_ref, w_ref = oracle.route(got_l, k, w.score_fn, w.normalize_topk, w.num_groups,
+                                  w.topk_groups, sb)
+    idx_gpu = host(b.topk_idx)
+    mism = np.argwhere(idx_gpu != idx_ref)
+    assert mism.size == 0, f"top-k ids differ at {mism[:5].tolist()}"
+    close(host(b.topk_w), w_ref, TOL_W, "combine weights")
+    # ---- dispatch tables from the GPU's own ids: bit-exact
+    d = oracle.dispatch(idx_gpu, E, w.num_ranks, w.rank_map, w.capacity_factor)
+    for name in ("expert_counts", "kept_counts", "expert_start", "rank_counts", "rank_offsets",
+                 "slot_of", "perm_src"):
+        np.testing.assert_array_equal(host(getattr(b, name)), d[name], err_msg=name)
+    nk = int(host(b.num_kept)[0])
+    assert nk == d["num_kept"]
+    assert host(b.expert_counts).sum() == N * k
+    # ---- send buffer rows are exact copies
+    ps = d["perm_src"][:nk]
+    xp = host(b.xperm[:nk])
+    np.testing.assert_array_equal(xp, x_h[ps // k], err_msg="xperm")
+    # ---- expert FFN on the GPU's send rows
+    flat_idx = idx_gpu.reshape(-1)
+    srows = np.arange(nk) if n_sample_rows is None else np.sort(
+        rng.choice(nk, size=min(nk, n_sample_rows), replace=False))
+    wgu, wd, sgu, sd = hw["w_gate_up"], hw["w_down"], hw["shared_gate_up"], hw["shared_down"]
+    if srows.size:
+        y_ref = oracle.expert_rows(xp[srows], flat_idx[ps[srows]], wgu, wd)
+        y_got = f64(b.yperm[torch.from_numpy(srows).cuda().long()])
+        close(y_got, y_ref, TOL_OUT[w.act_dtype], "expert FFN rows")
+    if sgu is not None:
+        trows = np.arange(N) if n_sample_rows is None else np.sort(
+            rng.choice(N, size=min(N, n_sample_rows), replace=False))
+        ys_ref = oracle.expert_rows(x_h[trows], np.full(trows.size, E, np.int32), wgu, wd, sgu, sd)
+        close(f64(b.yshared[torch.from_numpy(trows).cuda().long()]), ys_ref, TOL_OUT[w.act_dtype],
+              "shared expert rows")
+    # ---- combine from the GPU's yperm / weights, and the whole layer
+    slot = d["slot_of"].reshape(N, k)
+    dropped = np.nonzero((slot < 0).all(axis=1))[0]
+    if n_sample_tokens is None:
+        toks = np.arange(N)
+    else:
+        toks = np.unique(np.concatenate([rng.choice(N, size=min(N, n_sample_tokens), replace=False),
+                                         dropped[:32]]))
+    toks = toks.astype(np.int32)
+    ys_h = None if b.yshared is None else host(b.yshared)
+    out_got = f64(b.out)
+    c_ref = oracle.combine(toks, x_h, host(b.yperm), d["slot_of"],
+                           host(b.topk_w).astype(np.float64), ys_h)
+    close(out_got[toks], c_ref, TOL_COMBINE[w.act_dtype], "combine")
+    if w.shared_d_ff == 0 and dropped.size:
+        # a token whose every choice was dropped leaves the layer unchanged, bit for bit
+        np.testing.assert_array_equal(host(b.out)[dropped], x_h[dropped])
+    l_ref = oracle.layer_tokens(toks, x_h, idx_gpu, w_ref, d["slot_of"], wgu, wd, sgu, sd)
+    rel = close(out_got[toks], l_ref, TOL_OUT[w.act_dtype], "layer output")
+    return dict(rel_err=rel, drop_rate=1.0 - nk / (N * k), num_kept=nk)
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+@pytest.fixture(scope="module")
+def dsv3_inputs():
+    inp = W.make_inputs(W.DSV3_PREFILL, seed=0, device="cuda")
+    yield inp, host_weights(inp)
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_tiny_top2_f32_full():
+    w = W.TINY_TOP2_F32
+    inp = W.make_inputs(w, seed=0, device="cuda")
+    b, _ = run_gpu(w, inp)
+    check_layer(w, inp, b)
+    # the glossary page's printed ranges hold on the GPU's routing too
+    ec, rc = host(b.expert_counts), host(b.rank_counts)
+    assert (ec.min(), ec.max(), rc.min(), rc.max()) == (948, 1087, 1968, 2139)
+
+
+@pytest.mark.parametrize("w", [W.SWITCH_TOP1, W.GSHARD_TOP2], ids=lambda w: w.name)
+def test_capacity_workloads(w):
+    inp = W.make_inputs(w, seed=0, device="cuda")
+    b, _ = run_gpu(w, inp)
+    r = check_layer(w, inp, b, n_sample_tokens=256, n_sample_rows=256)
+    C = oracle.capacity(w.tokens, w.top_k, w.num_experts, w.capacity_factor)
+    assert host(b.kept_counts).max() <= C
+    print(f"{w.name}: drop rate {r['drop_rate']:.4f}, layer rel err {r['rel_err']:.2e}")
+
+
+def test_dsv3_prefill_and_bias_update(dsv3_inputs):
+    from expert_routing_router_b300 import moe
+    w, (inp, hw) = W.DSV3_PREFILL, dsv3_inputs
+    b, bias0 = run_gpu(w, inp)
+    check_layer(w, inp, b, n_sample_tokens=48, n_sample_rows=128, hw=hw)
+    counts = host(b.expert_counts)
+    moe.moe_bias_update(b.cfg, b.expert_counts, inp["sel_bias"], w.bias_step)
+    torch.cuda.synchronize()
+    ref = oracle.bias_update(counts, host(bias0), w.tokens, w.top_k, w.bias_step)
+    np.testing.assert_array_equal(host(inp["sel_bias"]), ref)
+    inp["sel_bias"].copy_(bias0)
+
+
+@pytest.mark.parametrize("T", W.DECODE_TOKENS)
+def test_dsv3_decode_sweep(dsv3_inputs, T):
+    w = W.DSV3_DECODE.with_tokens(T)
+    inp = dict(dsv3_inputs[0])
+    inp["x"] = W.make_tokens(w, T, seed=1, device="cuda")
+    b, _ = run_gpu(w, inp)
+    check_layer(w, inp, b, n_sample_tokens=None if T <= 8 else 8, n_sample_rows=64,
+                hw=dsv3_inputs[1])
+
+
+# ---------------------------------------------------------------- edge cases (small, full check)
+
+def small(**kw):
+    base = dict(name="edge", tokens=1000, hidden=264, num_experts=16, top_k=4, num_ranks=4,
+                rank_map=0, score_fn=1, normalize_topk=True, num_groups=4, topk_groups=2,
+                capacity_factor=0.0, d_ff=200, shared_d_ff=72, act_dtype="bf16",
+                router_offset_std=0.0, sel_bias_std=0.1, bias_step=1e-3, expert_std=0.05)
+    base.update(kw)
+    return W.Workload(**base)
+
+
+EDGE = {
+    "ragged_sigmoid_groups_shared": small(),
+    "ragged_f32_softmax_cap": small(tokens=777, hidden=136, num_experts=12, top_k=3, num_ranks=3,
+                                    score_fn=0, num_groups=1, topk_groups=1,
+                                    capacity_factor=1.0, d_ff=40, shared_d_ff=0,
+                                    act_dtype="f32", sel_bias_std=0.0),
+    "one_token": small(tokens=1, hidden=128, num_experts=64, top_k=8, num_ranks=8,
+                       num_groups=8, topk_groups=4, d_ff=64, shared_d_ff=64),
+    "dense_single_expert": small(tokens=300, hidden=64, num_experts=1, top_k=1, num_ranks=1,
+                                 score_fn=0, num_groups=1, topk_groups=1, d_ff=64,
+                                 shared_d_ff=0, sel_bias_std=0.0),
+    "k_equals_E": small(tokens=200, hidden=64, num_experts=4, top_k=4, num_ranks=2, score_fn=0,
+                        num_groups=1, topk_groups=1, d_ff=32, shared_d_ff=0, sel_bias_std=0.0),
+    "round_robin_uneven_ranks": small(tokens=513, hidden=96, num_experts=64, top_k=6,
+                                      num_ranks=40, rank_map=1, num_groups=1, topk_groups=1,
+                                      d_ff=48, shared_d_ff=0),
+    "tiny_capacity_most_dropped": small(tokens=640, hidden=64, num_experts=8, top_k=2,
+                                        num_ranks=2, score_fn=0, num_groups=1, topk_groups=1,
+                                        capacity_factor=0.05, d_ff=32, shared_d_ff=0,
+                                        sel_bias_std=0.0),
+    "capacity_exact_boundary": small(tokens=256, hidden=64, num_experts=4, top_k=1, num_ranks=4,
+                                     score_fn=0, num_groups=1, topk_groups=1,
+                                     capacity_factor=1.0, d_ff=32, shared_d_ff=0,
+                                     sel_bias_std=0.0, act_dtype="f32"),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_cases(name):
+    w = EDGE[name]
+    inp = W.make_inputs(w, seed=3, device="cuda")
+    b, _ = run_gpu(w, inp)
+    check_layer(w, inp, b)
+
+
+def test_all_tokens_to_one_expert_with_cap():
+    w = EDGE["tiny_capacity_most_dropped"]
+    w = dataclasses.replace(w, capacity_factor=1.0)
+    inp = W.make_inputs(w, seed=4, device="cuda")
+    inp["b_router"][5] += 100.0          # expert 5 is every token's first choice
+    b, _ = run_gpu(w, inp)
+    r = check_layer(w, inp, b)
+    assert host(b.expert_counts)[5] == w.tokens
+    assert host(b.kept_counts)[5] == oracle.capacity(w.tokens, w.top_k, w.num_experts, 1.0)
+
+
+def test_large_selection_bias_forces_choice_but_not_weights():
+    w = EDGE["ragged_sigmoid_groups_shared"]
+    inp = W.make_inputs(w, seed=5, device="cuda")
+    inp["sel_bias"][[1, 2]] = 50.0       # same group: that group and these two experts win
+    inp["sel_bias"][[9]] = -50.0         # never chosen
+    b, _ = run_gpu(w, inp)
+    check_layer(w, inp, b)
+    idx = host(b.topk_idx)
+    assert np.all(idx[:, 0:2] == [1, 2]) or np.all(np.sort(idx[:, :2], 1) == [1, 2])
+    assert not np.any(idx == 9)
