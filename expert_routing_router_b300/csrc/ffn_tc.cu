@@ -494,7 +494,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint3
 cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert_start,
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,
-                          void* yperm, void* yshared, void* h, void* sched, cudaStream_t s) {
+                          void* yperm, void* yshared, void* h, int* status, cudaStream_t s) {
   const bool sh = c.Fs > 0;
   __nv_bfloat16* h_routed = static_cast<__nv_bfloat16*>(h);
   __nv_bfloat16* h_shared = h_routed + (size_t)c.A * c.F;
@@ -506,7 +506,7 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
   b1 = b0;
   if (sh && (!make_map(&a1, x, c.d, c.N, BM) || !make_map(&b1, shared_gate_up, c.d, 2 * c.Fs, BN / 2)))
     return cudaErrorInvalidValue;
-  TcParams p{expert_start, kept_counts, h_routed, h_shared, static_cast<int*>(sched),
+  TcParams p{expert_start, kept_counts, h_routed, h_shared, status,
              c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
   const int grid = num_sms();
   auto k1 = grouped_ffn_kernel<GATE_UP>;

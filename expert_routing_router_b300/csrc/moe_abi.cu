@@ -98,6 +98,8 @@ size_t round_up(size_t v) { return (v + 255) & ~size_t(255); }
 WsLayout layout(const Cfg& c) {
   WsLayout w;
   size_t off = 0;
+  w.status = off;
+  off += 256;
   w.chunk_hist = off;
   off += round_up((size_t)c.n_chunks * c.E * sizeof(int32_t));
   w.h = off;
@@ -199,10 +201,15 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_
   if ((st = ws_check(c, workspace, workspace_bytes, &w)) != MOE_OK) return st;
   if ((st = check_device()) != MOE_OK) return st;
   void* h = static_cast<char*>(workspace) + w.h;
+  int* status = reinterpret_cast<int*>(static_cast<char*>(workspace) + w.status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const void* xs = c.Fs > 0 ? x : nullptr;
-  return from_cuda(launch_ffn_simt(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
-                                   shared_gate_up, shared_down, yperm, yshared, h, s));
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (c.act == MOE_DTYPE_F32)
+    return from_cuda(launch_ffn_simt(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
+                                     shared_gate_up, shared_down, yperm, yshared, h, s));
+  return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
+                                 shared_gate_up, shared_down, yperm, yshared, h, status, s));
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* yperm, const int32_t* slot_of,

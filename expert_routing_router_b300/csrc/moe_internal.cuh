@@ -26,9 +26,10 @@ struct Cfg {
 
 // Workspace carve-up (one layout serves every call).
 struct WsLayout {
+  size_t status;      // int32 device status word (0 = ok)
   size_t chunk_hist;  // [n_chunks, E] int32
   size_t h;           // FFN intermediate: [A, F] then [N, Fs], act dtype
-  size_t sched;       // tile scheduler scratch
+  size_t sched;       // reserved scratch
   size_t total;
 };
 
@@ -76,7 +77,7 @@ cudaError_t launch_ffn_simt(const Cfg& c, const void* xperm, const int32_t* expe
 cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert_start,
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,
-                          void* yperm, void* yshared, void* h, void* sched, cudaStream_t s);
+                          void* yperm, void* yshared, void* h, int* status, cudaStream_t s);
 cudaError_t launch_combine(const Cfg& c, const void* yperm, const int32_t* slot_of,
                            const float* topk_w, const void* residual, const void* yshared,
                            void* out, cudaStream_t s);

@@ -60,6 +60,8 @@ def run_gpu(w, inp):
     bias_before = None if inp["sel_bias"] is None else inp["sel_bias"].clone()
     moe.run_layer(b, inp)
     torch.cuda.synchronize()
+    # device status word (first int32 of the workspace): no kernel gave up a wait
+    assert int(b.workspace[:4].view(torch.int32).item()) == 0
     return b, bias_before
 
 
