@@ -1,0 +1,379 @@
+"""Benchmark of the MoE layer hot path on B300: route -> dispatch -> expert FFN -> combine
+(+ selection-bias update), through the C-ABI library.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl native|reference]
+
+One step = one pass of the whole path over one batch of seeded synthetic tokens of
+the named workload (default: the DeepSeek-V3-shaped prefill layer, 8192 tokens x
+7168, 256 routed experts top-8 + 1 shared, bf16).  Prints ONE JSON line on rank 0.
+
+  value        tokens/s over all ranks, from CUDA events around each timed step on
+               the launching stream (inputs resident in HBM; L2 flushed between steps
+               outside the events)
+  e2e          the same metric with the step's hidden states copied host->device from
+               pinned memory and the layer output copied back, inside the timed region
+  roofline     the expert grouped-GEMM pair (moe_expert_ffn) against measured bf16
+               tensor peak; dispatch+combine against measured HBM copy bandwidth
+  cpu_baseline the CPU oracle on a bounded token sample, on this host's cores
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU with
+its own tokens (weak scaling, no collective on the data path); the time is the max
+over ranks.  --impl reference times the CPU oracle (rank 0 only) on the same metric.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from expert_routing_router_b300 import workloads as W  # noqa: E402
+
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="dsv3_prefill",
+                    help="workload name; '<name>@<tokens>' changes the token count")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload(name):
+    base, _, n = name.partition("@")
+    w = W.WORKLOADS[base]
+    return w.with_tokens(int(n)) if n else w
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sust=p["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sust=1400.0, src="fallback")
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world <= 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank, steps, world, max_seconds):
+    """Whole-job tokens/s: every rank processed tokens_per_rank per step."""
+    return tokens_per_rank * steps * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", str(index)], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(0.5)
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = [r.split(", ") for r in open(self.f.name).read().strip().splitlines() if r]
+        os.unlink(self.f.name)
+        rows = [r for r in rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = np.array([float(r[1]) for r in rows])
+        mx = float(rows[0][2])
+        load = sm[sm > 0.5 * sm.max()] if sm.size else sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": float(np.median(load)), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def host(t):
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def oracle_inputs(inp):
+    return {k: (None if v is None else host(v)) for k, v in inp.items()}
+
+
+def oracle_step(oracle, w, h, n):
+    """One layer pass of the oracle over the first n tokens, as a batch of n."""
+    x = h["x"][:n]
+    logits = oracle.router_logits(x, h["w_router"], h["b_router"])
+    idx, wts = oracle.route(logits, w.top_k, w.score_fn, w.normalize_topk, w.num_groups,
+                            w.topk_groups, h["sel_bias"])
+    d = oracle.dispatch(idx, w.num_experts, w.num_ranks, w.rank_map, w.capacity_factor)
+    oracle.layer_tokens(np.arange(n, dtype=np.int32), x, idx, wts, d["slot_of"],
+                        h["w_gate_up"], h["w_down"], h["shared_gate_up"], h["shared_down"])
+    if w.bias_step and h["sel_bias"] is not None:
+        oracle.bias_update(d["expert_counts"], h["sel_bias"], n, w.top_k, w.bias_step)
+
+
+def oracle_sample_size(oracle, w, h, budget_s):
+    """Largest token sample whose oracle pass fits in about budget_s seconds (the
+    oracle runs tokens in parallel, so calibrate with one token per host thread)."""
+    n = max(2, min(w.tokens, oracle.num_threads()))
+    t0 = time.perf_counter()
+    oracle_step(oracle, w, h, n)
+    per_tok = (time.perf_counter() - t0) / n
+    return int(max(1, min(w.tokens, budget_s / max(per_tok, 1e-9))))
+
+
+def cpu_baseline(w, h, budget_s=15.0):
+    import oracle
+    n = oracle_sample_size(oracle, w, h, budget_s)
+    t0 = time.perf_counter()
+    oracle_step(oracle, w, h, n)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {n} of {w.tokens} tokens of {w.name} as one batch: fp64 router, "
+                      f"routing, dispatch, SwiGLU experts and combine ({dt:.1f} s)"}
+
+
+# ------------------------------------------------------------------ native arm
+def launches_per_step(w):
+    n = 1                      # route
+    n += 4                     # dispatch: count, scan, assign, permute
+    n += 2                     # expert FFN: gate_up and down grouped GEMMs
+    n += 1                     # combine
+    n += 1 if w.bias_step else 0
+    return n
+
+
+def algorithmic(w, num_kept):
+    """Bytes / flops the method must move or compute in one step."""
+    s = 2 if w.act_dtype == "bf16" else 4
+    N, d = w.tokens, w.hidden
+    ns = N if w.shared_d_ff else 0
+    dispatch_bytes = (N + num_kept) * d * s                 # read every token once, write kept rows
+    combine_bytes = (num_kept + N + ns + N) * d * s          # kept rows + residual + shared + out
+    flops = 6.0 * d * (w.d_ff * num_kept + w.shared_d_ff * ns)
+    return dispatch_bytes, combine_bytes, flops
+
+
+def run_native(a, w, rank, world, local):
+    from expert_routing_router_b300 import moe
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    inp = W.make_inputs(w, seed=a.seed + rank, device=dev)
+    b = moe.LayerBuffers(w, device=dev)
+    step_bias = w.bias_step
+    bias0 = None if inp["sel_bias"] is None else inp["sel_bias"].clone()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+
+    def step(evs=None):
+        c = b.cfg
+        if evs: evs[0].record(s)
+        moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"], b.logits,
+                      b.topk_idx, b.topk_w, b.workspace)
+        if evs: evs[1].record(s)
+        moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
+                         b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
+                         b.num_kept, b.workspace)
+        if evs: evs[2].record(s)
+        moe.moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
+                           inp["w_down"], inp["x"], inp["shared_gate_up"], inp["shared_down"],
+                           b.yperm, b.yshared, b.workspace)
+        if evs: evs[3].record(s)
+        moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out)
+        if evs: evs[4].record(s)
+        if step_bias and inp["sel_bias"] is not None:
+            moe.moe_bias_update(c, b.expert_counts, inp["sel_bias"], step_bias)
+        if evs: evs[5].record(s)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    if bias0 is not None:
+        inp["sel_bias"].copy_(bias0)
+    assert int(b.workspace[:4].view(torch.int32).item()) == 0, "device status word set"
+    num_kept = int(b.num_kept.item())
+
+    # ---------------- timed: K steps, per-step / per-call events on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(a.steps)]
+    clk = Clocks(dev.index) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        flush.fill_(i & 0xff)            # L2 flush, outside the step's events
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = clk.stop() if clk else None
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])  # ms
+    step_ms = per.sum(axis=1)
+    total_s = max_over_ranks(step_ms.sum() / 1e3, world)
+    value = weak_scaling_value(w.tokens, a.steps, world, total_s)
+    route_ms, disp_ms, ffn_ms, comb_ms, bias_ms = per.mean(axis=0)
+    status = int(b.workspace[:4].view(torch.int32).item())
+    if bias0 is not None:
+        inp["sel_bias"].copy_(bias0)
+
+    # ---------------- end to end through the C ABI with host buffers
+    x_host = torch.empty(w.tokens, w.hidden, dtype=w.torch_dtype, pin_memory=True)
+    x_host.copy_(inp["x"])
+    out_host = torch.empty_like(x_host, pin_memory=True)
+    x_dev = inp["x"]
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(a.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        step()
+        out_host.copy_(b.out, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = weak_scaling_value(w.tokens, a.steps, world, e2e_s)
+    if bias0 is not None:
+        inp["sel_bias"].copy_(bias0)
+    io_bytes = w.tokens * w.hidden * (2 if w.act_dtype == "bf16" else 4)
+
+    # ---------------- roofline figures
+    pk = peaks()
+    disp_b, comb_b, flops = algorithmic(w, num_kept)
+    ffn_tflops = flops / (ffn_ms * 1e-3) / 1e12
+    # dispatch+combine: bytes over (permute + combine) time; the dispatch call also
+    # holds the count / scan / assign kernels, included here (conservative)
+    dc_gbs = (disp_b + comb_b) / ((disp_ms + comb_ms) * 1e-3) / 1e9
+    out = {
+        "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": float(step_ms.mean()),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.act_dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
+                   "num_experts": w.num_experts, "top_k": w.top_k, "num_ranks": w.num_ranks,
+                   "d_ff": w.d_ff, "shared_d_ff": w.shared_d_ff,
+                   "capacity_factor": w.capacity_factor, "seed": a.seed,
+                   "l2": "flushed between steps (252 MiB write outside the step events); "
+                         "per-step working set larger than L2",
+                   "parallelism": f"replica x{world} (token-sharded, no collective)"},
+        "roofline": {"kernel": "expert grouped GEMMs (gate_up+SwiGLU, down) of moe_expert_ffn",
+                     "bound": "tensor", "achieved": ffn_tflops, "peak": pk["bf16_sust"],
+                     "unit": "TFLOP/s", "frac": ffn_tflops / pk["bf16_sust"],
+                     "peak_kind": f"{pk['src']} sustained bf16 (kernel timed inside the step)",
+                     "frac_of_burst": ffn_tflops / pk["bf16"], "traffic": None,
+                     "algorithmic_flops_per_launch": flops},
+        "dispatch_combine": {"bytes": disp_b + comb_b, "achieved": dc_gbs, "unit": "GB/s",
+                             "peak": pk["hbm"], "frac": dc_gbs / pk["hbm"],
+                             "frac_of_8TBs": dc_gbs / 8000.0},
+        "stage_ms": {"route": route_ms, "dispatch": disp_ms, "expert_ffn": ffn_ms,
+                     "combine": comb_ms, "bias_update": bias_ms},
+        "routing": {"num_kept": num_kept, "drop_rate": 1.0 - num_kept / (w.tokens * w.top_k)},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
+                "d2h_bytes_per_step": io_bytes},
+        "clocks": clocks, "gpu_launches": launches_per_step(w) * a.steps,
+        "device_status": status,
+    }
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        del b, flush
+        torch.cuda.empty_cache()
+        out["cpu_baseline"] = cpu_baseline(w, oracle_inputs(inp))
+    return out
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(a, w):
+    """The CPU oracle as it stands, on this host's cores: same workload, metric, unit."""
+    import oracle
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    h = oracle_inputs(W.make_inputs(w, seed=a.seed, device=dev))
+    budget = 120.0 / max(1, a.steps + a.warmup)
+    n = oracle_sample_size(oracle, w, h, budget)
+    for _ in range(a.warmup):
+        oracle_step(oracle, w, h, n)
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        oracle_step(oracle, w, h, n)
+    dt = time.perf_counter() - t0
+    value = n * a.steps / dt
+    sample = (f"each step: first {n} of {w.tokens} tokens of {w.name} as one batch through the "
+              f"fp64 CPU oracle (router, routing, dispatch, SwiGLU experts, combine)")
+    return {"impl": "reference", "metric": "MoE-layer tokens/s", "value": value,
+            "unit": "tokens/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
+                       "num_experts": w.num_experts, "top_k": w.top_k, "sample_tokens": n},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    a = parse()
+    w = workload(a.config)
+    if a.impl == "reference":
+        # rank 0 alone times the CPU oracle; other ranks exit without work
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_reference(a, w)), flush=True)
+        return
+    rank, world, local = dist_setup(a.gpus)
+    out = run_native(a, w, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
