@@ -179,6 +179,29 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const vo
                                    static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                                void* xperm, int32_t* expert_counts, int32_t* kept_counts,
+                                int32_t* expert_start, int32_t* rank_counts,
+                                int32_t* rank_offsets, int32_t* slot_of, int32_t* perm_src,
+                                int32_t* num_kept, void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!topk_idx || !expert_counts || !kept_counts || !expert_start || !rank_counts ||
+      !rank_offsets || !slot_of || !perm_src || !num_kept)
+    return MOE_ERR_INVALID_ARG;
+  if (xperm && (!x || !aligned(x, 16) || !aligned(xperm, 16))) return MOE_ERR_INVALID_ARG;
+  const void* ints[] = {topk_idx, expert_counts, kept_counts, expert_start, rank_counts,
+                        rank_offsets, slot_of, perm_src, num_kept};
+  for (const void* p : ints)
+    if (!aligned(p, 4)) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)c.n_chunks * c.E > kNoAllocHistInts) return MOE_ERR_WORKSPACE;
+  if ((st = check_device()) != MOE_OK) return st;
+  return from_cuda(launch_dispatch_noalloc(c, topk_idx, x, xperm, expert_counts, kept_counts,
+                                           expert_start, rank_counts, rank_offsets, slot_of,
+                                           perm_src, num_kept, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_t* expert_start,
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,

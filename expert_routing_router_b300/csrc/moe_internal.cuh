@@ -13,6 +13,8 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxGroups = 32;
 constexpr int kChunk = 2048;  // assignments per dispatch chunk (counting / slot pass)
+// Static scratch of moe_dispatch_noalloc: per-chunk histogram, n_chunks * E int32.
+constexpr int kNoAllocHistInts = 65536;
 
 // ---------------------------------------------------------------- host-side view
 struct Cfg {
@@ -70,6 +72,11 @@ cudaError_t launch_dispatch(const Cfg& c, const int32_t* topk_idx, const void* x
                             int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
                             int32_t* perm_src, int32_t* num_kept, int32_t* chunk_hist,
                             cudaStream_t s);
+cudaError_t launch_dispatch_noalloc(const Cfg& c, const int32_t* topk_idx, const void* x,
+                                    void* xperm, int32_t* expert_counts, int32_t* kept_counts,
+                                    int32_t* expert_start, int32_t* rank_counts,
+                                    int32_t* rank_offsets, int32_t* slot_of, int32_t* perm_src,
+                                    int32_t* num_kept, cudaStream_t s);
 cudaError_t launch_ffn_simt(const Cfg& c, const void* xperm, const int32_t* expert_start,
                             const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                             const void* x, const void* shared_gate_up, const void* shared_down,

@@ -34,8 +34,8 @@ class MoeError(RuntimeError):
         super().__init__(f"{fn} failed: {status_string(status)}")
 
 
-EXPORTS = ("moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
-           "moe_bias_update", "moe_status_string")
+EXPORTS = ("moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc",
+           "moe_expert_ffn", "moe_combine", "moe_bias_update", "moe_status_string")
 
 
 def _load():
@@ -48,6 +48,7 @@ def _load():
     lib.moe_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_route.argtypes = [C] + [P] * 8 + [S, P]
     lib.moe_dispatch.argtypes = [C] + [P] * 12 + [S, P]
+    lib.moe_dispatch_noalloc.argtypes = [C] + [P] * 11 + [P]
     lib.moe_expert_ffn.argtypes = [C] + [P] * 11 + [S, P]
     lib.moe_combine.argtypes = [C] + [P] * 6 + [P]
     lib.moe_bias_update.argtypes = [C, P, P, F, P]
@@ -114,6 +115,16 @@ def moe_dispatch(cfg, topk_idx, x, xperm, expert_counts, kept_counts, expert_sta
         _p(expert_start), _p(rank_counts), _p(rank_offsets), _p(slot_of), _p(perm_src),
         _p(num_kept), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def moe_dispatch_noalloc(cfg, topk_idx, x, xperm, expert_counts, kept_counts, expert_start,
+                         rank_counts, rank_offsets, slot_of, perm_src, num_kept, stream=None):
+    """moe_dispatch for callers that cannot allocate: no workspace argument; the scratch
+    is a static array inside the library (see include/moe.h for limits and caveats)."""
+    _check("moe_dispatch_noalloc", _lib.moe_dispatch_noalloc(
+        ctypes.byref(cfg), _p(topk_idx), _p(x), _p(xperm), _p(expert_counts), _p(kept_counts),
+        _p(expert_start), _p(rank_counts), _p(rank_offsets), _p(slot_of), _p(perm_src),
+        _p(num_kept), _stream(stream)))
 
 
 def moe_expert_ffn(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x, shared_gate_up,

@@ -148,6 +148,27 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, 
                         int32_t* slot_of, int32_t* perm_src, int32_t* num_kept,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* Dispatch without any device allocation by the caller.  The pages have no
+ * counterpart to this call; it exists for callers that cannot call cudaMalloc or
+ * own a workspace -- for example a runtime whose memory is planned ahead of time by
+ * an allocator it does not control, or code on a path where an allocation (which may
+ * synchronise the device) is not allowed.  Same arguments, results and ordering as
+ * moe_dispatch, minus the workspace: its scratch (a per-chunk expert histogram of
+ * ceil(N*k / 2048) * num_experts int32) lives in a static device array of 65536
+ * int32 (256 KiB) inside the library, which every GPU that loads the library keeps
+ * until the process exits.  Larger layers are rejected with MOE_ERR_WORKSPACE (use
+ * moe_dispatch).  The first call on a device looks up the array's device address
+ * with that device current; make that first call before any stream capture.  All
+ * calls share the one array: calls that overlap on the GPU (on different streams)
+ * race and give wrong results.  Leftover contents from an earlier call are never
+ * read, so nothing needs clearing.  Allocates nothing. */
+MOE_API moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx,
+                                        const void* x, void* xperm, int32_t* expert_counts,
+                                        int32_t* kept_counts, int32_t* expert_start,
+                                        int32_t* rank_counts, int32_t* rank_offsets,
+                                        int32_t* slot_of, int32_t* perm_src, int32_t* num_kept,
+                                        void* stream);
+
 /* Expert compute.  Same page, step 3 (each rank runs its local experts on the
  * tokens it received); fudan-mlsys-cn chapter 10, section 10.5 (a shared expert sees
  * every token).  Each expert is a SwiGLU feed-forward block:
