@@ -100,6 +100,14 @@ WsLayout layout(const Cfg& c) {
   size_t off = 0;
   w.status = off;
   off += 256;
+  w.router_w = off;
+  w.router_partial = off;
+  if (c.act == MOE_DTYPE_BF16) {
+    const RouterPlan rp = router_plan(c);
+    off += round_up(rp.ws_bytes);
+    w.router_partial = off;
+    off += round_up(rp.partial_bytes);
+  }
   w.chunk_hist = off;
   off += round_up((size_t)c.n_chunks * c.E * sizeof(int32_t));
   w.h = off;
@@ -150,7 +158,10 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* w_router
   WsLayout w;
   if ((st = ws_check(c, workspace, workspace_bytes, &w)) != MOE_OK) return st;
   if ((st = check_device()) != MOE_OK) return st;
+  char* ws = static_cast<char*>(workspace);
   return from_cuda(launch_route(c, x, w_router, b_router, sel_bias, logits, topk_idx, topk_w,
+                                ws + w.router_w, reinterpret_cast<float*>(ws + w.router_partial),
+                                reinterpret_cast<int*>(ws + w.status),
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -227,7 +238,6 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_
   int* status = reinterpret_cast<int*>(static_cast<char*>(workspace) + w.status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const void* xs = c.Fs > 0 ? x : nullptr;
-  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (c.act == MOE_DTYPE_F32)
     return from_cuda(launch_ffn_simt(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
                                      shared_gate_up, shared_down, yperm, yshared, h, s));

@@ -26,9 +26,20 @@ struct Cfg {
   int act_bytes;   // 4 (fp32) or 2 (bf16)
 };
 
+// Tensor-core router: padded sizes and the K slicing of its GEMM.
+struct RouterPlan {
+  int Epad, dpad, kb_per_split, nsplit;
+  int n_acc, acc_cols;   // TMEM accumulators per CTA and columns per accumulator
+  size_t ws_bytes;       // bf16 3-term split of the router weight [Epad, 3*dpad]
+  size_t partial_bytes;  // fp32 partial logits [nsplit, N, Epad]
+};
+constexpr int kSmTarget = 148;  // SM count the router slicing is planned for
+
 // Workspace carve-up (one layout serves every call).
 struct WsLayout {
   size_t status;      // int32 device status word (0 = ok)
+  size_t router_w;    // RouterPlan::ws_bytes
+  size_t router_partial;  // RouterPlan::partial_bytes
   size_t chunk_hist;  // [n_chunks, E] int32
   size_t h;           // FFN intermediate: [A, F] then [N, Fs], act dtype
   size_t sched;       // reserved scratch
@@ -66,7 +77,11 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
 namespace moe {
 cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, const float* b_router,
                          const float* sel_bias, float* logits, int32_t* topk_idx, float* topk_w,
-                         cudaStream_t s);
+                         void* ws_split, float* partial, int* status, cudaStream_t s);
+RouterPlan router_plan(const Cfg& c);
+cudaError_t launch_router_gemm(const Cfg& c, const RouterPlan& rp, const void* x,
+                               const float* w_router, void* ws_split, float* partial, int* status,
+                               cudaStream_t s);
 cudaError_t launch_dispatch(const Cfg& c, const int32_t* topk_idx, const void* x, void* xperm,
                             int32_t* expert_counts, int32_t* kept_counts, int32_t* expert_start,
                             int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,

@@ -91,81 +91,16 @@ struct RouteParams {
   int N, d, E, k, score_fn, normalize, G, TG;
 };
 
-template <typename T>
-__global__ void __launch_bounds__(THREADS)
-route_kernel(const T* __restrict__ x, const float* __restrict__ W, const float* __restrict__ b,
-             const float* __restrict__ sel_bias, float* __restrict__ logits,
-             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteParams p) {
-  extern __shared__ float smem[];
+// Selection for the tokens of one tile whose logits sit in shared memory
+// (lt[r * EP + e] for r < TM), one warp per token: score, optional group limit, k
+// rounds of warp-shuffle arg-max, combine weights.  All threads of the CTA call it.
+__device__ void select_tile(float* lt, int EP, int t0, const RouteParams& p,
+                            const float* __restrict__ sel_bias, int32_t* __restrict__ topk_idx,
+                            float* __restrict__ topk_w) {
   const int E = p.E;
-  const int EP = E + 1;                       // padded row of the logits tile
-  float* xs = smem;                           // [TM][KC + 1]
-  float* ws = smem + TM * (KC + 1);           // [E][KC + 1]
-  float* lt = smem;                           // phase 2: [TM][E + 1] (reuses phase-1 space)
-
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int t0 = blockIdx.x * TM;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int EJ = (E + 31) / 32;
-
-  // ---------------- phase 1: logits tile
-  float acc[4][MAXJ];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < MAXJ; ++j) acc[i][j] = 0.0f;
-
-  for (int k0 = 0; k0 < p.d; k0 += KC) {
-    __syncthreads();
-    for (int q = tid; q < TM * KC; q += THREADS) {
-      const int r = q / KC, c = q % KC;
-      const int t = t0 + r, kk = k0 + c;
-      xs[r * (KC + 1) + c] = (t < p.N && kk < p.d) ? to_f32(x[(int64_t)t * p.d + kk]) : 0.0f;
-    }
-    for (int q = tid; q < E * KC; q += THREADS) {
-      const int e = q / KC, c = q % KC;
-      const int kk = k0 + c;
-      ws[e * (KC + 1) + c] = (kk < p.d) ? W[(int64_t)e * p.d + kk] : 0.0f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int c = 0; c < KC; ++c) {
-      float xv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) xv[i] = xs[(warp * 4 + i) * (KC + 1) + c];
-#pragma unroll
-      for (int j = 0; j < MAXJ; ++j) {
-        if (j < EJ) {
-          const int e = lane + 32 * j;
-          const float wv = (e < E) ? ws[e * (KC + 1) + c] : 0.0f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i][j] = fmaf(xv[i], wv, acc[i][j]);
-        }
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---------------- phase 2a: bias, logits out
-#pragma unroll
-  for (int j = 0; j < MAXJ; ++j) {
-    const int e = lane + 32 * j;
-    if (j < EJ && e < E) {
-      const float be = b ? b[e] : 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) lt[(warp * 4 + i) * EP + e] = acc[i][j] + be;
-    }
-  }
-  __syncthreads();
-  for (int q = tid; q < TM * E; q += THREADS) {
-    const int r = q / E, e = q % E;
-    const int t = t0 + r;
-    if (t < p.N) logits[(int64_t)t * E + e] = lt[r * EP + e];
-  }
-  __syncthreads();  // rows are overwritten with ranking keys below
-
-  // ---------------- phase 2b: selection, one warp per token
   const int gs = E / p.G;
   for (int r = warp; r < TM; r += THREADS / 32) {
     const int t = t0 + r;
@@ -277,27 +212,133 @@ route_kernel(const T* __restrict__ x, const float* __restrict__ W, const float* 
   }
 }
 
+template <typename T>
+__global__ void __launch_bounds__(THREADS)
+route_kernel(const T* __restrict__ x, const float* __restrict__ W, const float* __restrict__ b,
+             const float* __restrict__ sel_bias, float* __restrict__ logits,
+             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteParams p) {
+  extern __shared__ float smem[];
+  const int E = p.E;
+  const int EP = E + 1;                       // padded row of the logits tile
+  float* xs = smem;                           // [TM][KC + 1]
+  float* ws = smem + TM * (KC + 1);           // [E][KC + 1]
+  float* lt = smem;                           // phase 2: [TM][E + 1] (reuses phase-1 space)
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int t0 = blockIdx.x * TM;
+  const int EJ = (E + 31) / 32;
+
+  // ---------------- phase 1: logits tile
+  float acc[4][MAXJ];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < MAXJ; ++j) acc[i][j] = 0.0f;
+
+  for (int k0 = 0; k0 < p.d; k0 += KC) {
+    __syncthreads();
+    for (int q = tid; q < TM * KC; q += THREADS) {
+      const int r = q / KC, c = q % KC;
+      const int t = t0 + r, kk = k0 + c;
+      xs[r * (KC + 1) + c] = (t < p.N && kk < p.d) ? to_f32(x[(int64_t)t * p.d + kk]) : 0.0f;
+    }
+    for (int q = tid; q < E * KC; q += THREADS) {
+      const int e = q / KC, c = q % KC;
+      const int kk = k0 + c;
+      ws[e * (KC + 1) + c] = (kk < p.d) ? W[(int64_t)e * p.d + kk] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < KC; ++c) {
+      float xv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xv[i] = xs[(warp * 4 + i) * (KC + 1) + c];
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j) {
+        if (j < EJ) {
+          const int e = lane + 32 * j;
+          const float wv = (e < E) ? ws[e * (KC + 1) + c] : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i][j] = fmaf(xv[i], wv, acc[i][j]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---------------- phase 2a: bias, logits out
+#pragma unroll
+  for (int j = 0; j < MAXJ; ++j) {
+    const int e = lane + 32 * j;
+    if (j < EJ && e < E) {
+      const float be = b ? b[e] : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lt[(warp * 4 + i) * EP + e] = acc[i][j] + be;
+    }
+  }
+  __syncthreads();
+  for (int q = tid; q < TM * E; q += THREADS) {
+    const int r = q / E, e = q % E;
+    const int t = t0 + r;
+    if (t < p.N) logits[(int64_t)t * E + e] = lt[r * EP + e];
+  }
+  __syncthreads();  // rows are overwritten with ranking keys below
+
+  select_tile(lt, EP, t0, p, sel_bias, topk_idx, topk_w);
+}
+
+// Router logits from the tensor-core path: fixed-order sum of the K slices plus the
+// router bias, written out, then the same selection as the SIMT path.
+__global__ void __launch_bounds__(THREADS)
+select_kernel(const float* __restrict__ partial, int nsplit, int Epad, const float* __restrict__ b,
+              const float* __restrict__ sel_bias, float* __restrict__ logits,
+              int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteParams p) {
+  extern __shared__ float smem[];
+  const int E = p.E, EP = E + 1;
+  float* lt = smem;
+  const int t0 = blockIdx.x * TM;
+  for (int q = threadIdx.x; q < TM * E; q += THREADS) {
+    const int r = q / E, e = q % E;
+    const int t = t0 + r;
+    if (t < p.N) {
+      float v = partial[(int64_t)t * Epad + e];
+      for (int sp = 1; sp < nsplit; ++sp) v += partial[((int64_t)sp * p.N + t) * Epad + e];
+      v += b ? b[e] : 0.0f;
+      lt[r * EP + e] = v;
+      logits[(int64_t)t * E + e] = v;
+    }
+  }
+  __syncthreads();
+  select_tile(lt, EP, t0, p, sel_bias, topk_idx, topk_w);
+}
+
 }  // namespace
 
 cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, const float* b_router,
                          const float* sel_bias, float* logits, int32_t* topk_idx, float* topk_w,
-                         cudaStream_t s) {
+                         void* ws_split, float* partial, int* status, cudaStream_t s) {
   RouteParams p{c.N, c.d, c.E, c.k, c.score_fn, c.normalize, c.G, c.TG};
-  const size_t sm1 = (size_t)(TM * (KC + 1) + c.E * (KC + 1)) * sizeof(float);
-  const size_t sm2 = (size_t)TM * (c.E + 1) * sizeof(float);
-  const size_t smem = sm1 > sm2 ? sm1 : sm2;
   const dim3 grid((c.N + TM - 1) / TM);
+  const size_t sm_sel = (size_t)TM * (c.E + 1) * sizeof(float);
   if (c.act == MOE_DTYPE_F32) {
+    // fp32 hidden states: fp32 FMAs on the CUDA cores, selection fused
+    const size_t sm1 = (size_t)(TM * (KC + 1) + c.E * (KC + 1)) * sizeof(float);
+    const size_t smem = sm1 > sm_sel ? sm1 : sm_sel;
     auto kern = route_kernel<float>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<grid, THREADS, smem, s>>>(static_cast<const float*>(x), w_router, b_router, sel_bias,
                                      logits, topk_idx, topk_w, p);
-  } else {
-    auto kern = route_kernel<__nv_bfloat16>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<grid, THREADS, smem, s>>>(static_cast<const __nv_bfloat16*>(x), w_router, b_router,
-                                     sel_bias, logits, topk_idx, topk_w, p);
+    return cudaGetLastError();
   }
+  // bf16 hidden states: tensor-core GEMM over the 3-term bf16 split of the weight
+  const RouterPlan rp = router_plan(c);
+  cudaError_t e = launch_router_gemm(c, rp, x, w_router, ws_split, partial, status, s);
+  if (e != cudaSuccess) return e;
+  cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_sel);
+  select_kernel<<<grid, THREADS, sm_sel, s>>>(partial, rp.nsplit, rp.Epad, b_router, sel_bias,
+                                              logits, topk_idx, topk_w, p);
   return cudaGetLastError();
 }
 

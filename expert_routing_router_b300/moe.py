@@ -171,6 +171,7 @@ class LayerBuffers:
         self.num_kept = torch.empty(1, **i32)
         nbytes = moe_workspace_size(self.cfg)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.workspace[:256].zero_()          # sticky device status word starts at 0
 
 
 def run_layer(b, inp, bias_step=0.0, stream=None):

@@ -91,11 +91,12 @@ typedef struct {
 /* Bytes of workspace that every call below needs for `cfg` (one size serves all
  * calls; a larger workspace is fine).  `bytes` is a HOST pointer.  The workspace is
  * device memory, 256-byte aligned, owned by the caller; its contents on entry do not
- * matter and on exit are unspecified, except for the device status word: the first
- * int32 of the workspace is set to 0 by moe_expert_ffn and becomes nonzero only if
- * one of its kernels gave up a bounded internal wait (its outputs are then invalid);
- * read it after the stream has reached the end of the call.  Calls sharing one
- * workspace must not overlap on the GPU. */
+ * matter and on exit are unspecified, except for the first int32, a sticky device
+ * status word: zero it once after allocating the workspace; a kernel of moe_route
+ * or moe_expert_ffn that gives up a bounded internal wait sets it nonzero (that
+ * call's outputs are then invalid) and no call clears it.  Read it once the stream
+ * has passed the calls of interest.  Calls sharing one workspace must not overlap
+ * on the GPU. */
 MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Routing.  Ultralytics glossary "Expert Parallelism", section "How tokens move
