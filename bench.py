@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="issue the C-ABI calls every step instead of replaying a CUDA graph")
     return ap.parse_args()
 
 
@@ -244,23 +246,49 @@ def run_native(a, w, rank, world, local):
     assert int(b.workspace[:4].view(torch.int32).item()) == 0, "device status word set"
     num_kept = int(b.num_kept.item())
 
-    # ---------------- timed: K steps, per-step / per-call events on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(a.steps)]
+    # one step captured as a CUDA graph (the five C-ABI calls, launched once each)
+    graph = None
+    if not a.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(a.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        if bias0 is not None:
+            inp["sel_bias"].copy_(bias0)
+    run = graph.replay if graph is not None else step
+
+    # ---------------- timed: K steps, CUDA events around each step on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(a.steps)]
     clk = Clocks(dev.index) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
     for i in range(a.steps):
         flush.fill_(i & 0xff)            # L2 flush, outside the step's events
-        step(evs[i])
+        evs[i][0].record(s)
+        run()
+        evs[i][1].record(s)
     torch.cuda.synchronize()
     barrier(world)
     clocks = clk.stop() if clk else None
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])  # ms
-    step_ms = per.sum(axis=1)
+    step_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
     total_s = max_over_ranks(step_ms.sum() / 1e3, world)
     value = weak_scaling_value(w.tokens, a.steps, world, total_s)
-    route_ms, disp_ms, ffn_ms, comb_ms, bias_ms = per.mean(axis=0)
     status = int(b.workspace[:4].view(torch.int32).item())
+    if bias0 is not None:
+        inp["sel_bias"].copy_(bias0)
+
+    # ---------------- per-stage times: direct C-ABI calls with events between calls
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(a.steps)]
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        flush.fill_(i & 0xff)
+        step(sevs[i])
+    torch.cuda.synchronize()
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in sevs])  # ms
+    route_ms, disp_ms, ffn_ms, comb_ms, bias_ms = per.mean(axis=0)
     if bias0 is not None:
         inp["sel_bias"].copy_(bias0)
 
@@ -275,7 +303,7 @@ def run_native(a, w, rank, world, local):
     e0.record(s)
     for i in range(a.steps):
         x_dev.copy_(x_host, non_blocking=True)
-        step()
+        run()
         out_host.copy_(b.out, non_blocking=True)
     e1.record(s)
     torch.cuda.synchronize()
@@ -304,7 +332,9 @@ def run_native(a, w, rank, world, local):
                    "capacity_factor": w.capacity_factor, "seed": a.seed,
                    "l2": "flushed between steps (252 MiB write outside the step events); "
                          "per-step working set larger than L2",
-                   "parallelism": f"replica x{world} (token-sharded, no collective)"},
+                   "parallelism": f"replica x{world} (token-sharded, no collective)",
+                   "launch": "CUDA graph of the five C-ABI calls" if graph is not None
+                             else "direct C-ABI calls"},
         "roofline": {"kernel": "expert grouped GEMMs (gate_up+SwiGLU, down) of moe_expert_ffn",
                      "bound": "tensor", "achieved": ffn_tflops, "peak": pk["bf16_sust"],
                      "unit": "TFLOP/s", "frac": ffn_tflops / pk["bf16_sust"],
@@ -315,7 +345,8 @@ def run_native(a, w, rank, world, local):
                              "peak": pk["hbm"], "frac": dc_gbs / pk["hbm"],
                              "frac_of_8TBs": dc_gbs / 8000.0},
         "stage_ms": {"route": route_ms, "dispatch": disp_ms, "expert_ffn": ffn_ms,
-                     "combine": comb_ms, "bias_update": bias_ms},
+                     "combine": comb_ms, "bias_update": bias_ms,
+                     "note": "direct calls with events between them (not graph replay)"},
         "routing": {"num_kept": num_kept, "drop_rate": 1.0 - num_kept / (w.tokens * w.top_k)},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                 "d2h_bytes_per_step": io_bytes},

@@ -26,8 +26,8 @@ def _deps():
     return glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
 
 
-def _compile(src, extra, verbose):
-    obj = os.path.join(OBJ, os.path.basename(src) + ".o")
+def _compile(src, extra, verbose, obj_dir=OBJ):
+    obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
     newest = max(os.path.getmtime(p) for p in [src] + _deps())
     if os.path.exists(obj) and os.path.getmtime(obj) >= newest and not extra:
         return obj
@@ -40,17 +40,18 @@ def _compile(src, extra, verbose):
     return obj
 
 
-def build(verbose=False, extra=()):
-    os.makedirs(OBJ, exist_ok=True)
+def build(verbose=False, extra=(), lib=LIB, obj_dir=OBJ):
+    """Build `lib` (default: the in-tree libmoe.so); `extra` adds nvcc flags."""
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, list(extra), verbose), srcs))
-    if (not os.path.exists(LIB) or extra
-            or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs)):
-        cmd = [NVCC] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", LIB + ".tmp"] + objs
+        objs = list(ex.map(lambda s: _compile(s, list(extra), verbose, obj_dir), srcs))
+    if (not os.path.exists(lib) or extra
+            or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs)):
+        cmd = [NVCC] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", lib + ".tmp"] + objs
         subprocess.run(cmd, check=True)
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":

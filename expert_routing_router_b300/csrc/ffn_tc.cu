@@ -120,6 +120,29 @@ __device__ __forceinline__ Tile decode(const Ctl* ctl, int nseg, int t) {
   return tl;
 }
 
+// TMA coordinates of one tile: A rows (segment rows), B rows (weights), K extent.
+struct Loads {
+  bool routed;
+  int K, a_row, b_row, b_row2;
+};
+
+template <int MODE>
+__device__ __forceinline__ Loads loads(const Tile& tl, const TcParams& p) {
+  Loads l;
+  l.routed = tl.seg < p.E;
+  const int Fx = l.routed ? p.F : p.Fs;
+  l.K = (MODE == GATE_UP) ? p.d : Fx;
+  l.a_row = tl.row_base + tl.m0;
+  if (MODE == GATE_UP) {
+    l.b_row = (l.routed ? tl.seg * 2 * p.F : 0) + tl.n0;
+    l.b_row2 = l.b_row + Fx;
+  } else {
+    l.b_row = (l.routed ? tl.seg * p.d : 0) + tl.n0;
+    l.b_row2 = 0;
+  }
+  return l;
+}
+
 // ---------------------------------------------------------------- kernel
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -194,21 +217,10 @@ grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_consta
       uint32_t armed = 0, armed_parity = 0;  // per-stage bits, for the abort drain
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode<MODE>(ctl, nseg, t);
-        const bool routed = tl.seg < p.E;
-        const int Fx = routed ? p.F : p.Fs;
-        const int K = (MODE == GATE_UP) ? p.d : Fx;
-        const CUtensorMap* ma = routed ? &tmA0 : &tmA1;
-        const CUtensorMap* mb = routed ? &tmB0 : &tmB1;
-        const int a_row = tl.row_base + tl.m0;
-        int b_row, b_row2 = 0;
-        if (MODE == GATE_UP) {
-          b_row = (routed ? tl.seg * 2 * p.F : 0) + tl.n0;
-          b_row2 = b_row + Fx;
-        } else {
-          b_row = (routed ? tl.seg * p.d : 0) + tl.n0;
-        }
-        for (int k0 = 0; k0 < K; k0 += BK) {
+        const Loads ld = loads<MODE>(decode<MODE>(ctl, nseg, t), p);
+        const CUtensorMap* ma = ld.routed ? &tmA0 : &tmA1;
+        const CUtensorMap* mb = ld.routed ? &tmB0 : &tmB1;
+        for (int k0 = 0; k0 < ld.K; k0 += BK) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1, ctl, p.err, 1)) {
             ok = false;
             break;
@@ -216,12 +228,12 @@ grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_consta
           uint8_t* sa = smem + (size_t)stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
-          tma_load(sa, ma, &ctl->full[stage], k0, a_row);
+          tma_load(sa, ma, &ctl->full[stage], k0, ld.a_row);
           if (MODE == GATE_UP) {
-            tma_load(sb, mb, &ctl->full[stage], k0, b_row);
-            tma_load(sb + B_BYTES / 2, mb, &ctl->full[stage], k0, b_row2);
+            tma_load(sb, mb, &ctl->full[stage], k0, ld.b_row);
+            tma_load(sb + B_BYTES / 2, mb, &ctl->full[stage], k0, ld.b_row2);
           } else {
-            tma_load(sb, mb, &ctl->full[stage], k0, b_row);
+            tma_load(sb, mb, &ctl->full[stage], k0, ld.b_row);
           }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -420,7 +432,15 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
              c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
   const int grid = num_sms();
   auto k1 = grouped_ffn_kernel<GATE_UP>;
-  cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  auto k2 = grouped_ffn_kernel<DOWN>;
+  static bool attr_set[64];  // function attributes once per device, outside stream capture
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    attr_set[dev & 63] = true;
+  }
   k1<<<grid, THREADS, SMEM_BYTES, s>>>(a0, a1, b0, b1, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -433,8 +453,6 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
     return cudaErrorInvalidValue;
   p.out0 = static_cast<__nv_bfloat16*>(yperm);
   p.out1 = static_cast<__nv_bfloat16*>(yshared);
-  auto k2 = grouped_ffn_kernel<DOWN>;
-  cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   k2<<<grid, THREADS, SMEM_BYTES, s>>>(a0, a1, b0, b1, p);
   return cudaGetLastError();
 }

@@ -241,6 +241,11 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_
   if (c.act == MOE_DTYPE_F32)
     return from_cuda(launch_ffn_simt(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
                                      shared_gate_up, shared_down, yperm, yshared, h, s));
+  // few rows per expert (decode): token-major kernel with right-sized token loads
+  if (c.A < (int64_t)kSmallRowsPerExpert * c.E)
+    return from_cuda(launch_ffn_tc_small(c, xperm, expert_start, kept_counts, w_gate_up, w_down,
+                                         xs, shared_gate_up, shared_down, yperm, yshared, h,
+                                         status, s));
   return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
                                  shared_gate_up, shared_down, yperm, yshared, h, status, s));
 }

@@ -100,6 +100,17 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,
                           void* yperm, void* yshared, void* h, int* status, cudaStream_t s);
+cudaError_t launch_ffn_tc_small(const Cfg& c, const void* xperm, const int32_t* expert_start,
+                                const int32_t* kept_counts, const void* w_gate_up,
+                                const void* w_down, const void* x, const void* shared_gate_up,
+                                const void* shared_down, void* yperm, void* yshared, void* h,
+                                int* status, cudaStream_t s);
+// Average send-buffer rows per expert below which the token-major small-segment
+// expert kernel is used (decode-sized batches).
+#ifndef MOE_SMALL_ROWS
+#define MOE_SMALL_ROWS 4
+#endif
+constexpr int kSmallRowsPerExpert = MOE_SMALL_ROWS;
 cudaError_t launch_combine(const Cfg& c, const void* yperm, const int32_t* slot_of,
                            const float* topk_w, const void* residual, const void* yshared,
                            void* out, cudaStream_t s);

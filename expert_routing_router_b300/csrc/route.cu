@@ -327,7 +327,8 @@ cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, con
     const size_t sm1 = (size_t)(TM * (KC + 1) + c.E * (KC + 1)) * sizeof(float);
     const size_t smem = sm1 > sm_sel ? sm1 : sm_sel;
     auto kern = route_kernel<float>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<grid, THREADS, smem, s>>>(static_cast<const float*>(x), w_router, b_router, sel_bias,
                                      logits, topk_idx, topk_w, p);
     return cudaGetLastError();
@@ -336,7 +337,8 @@ cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, con
   const RouterPlan rp = router_plan(c);
   cudaError_t e = launch_router_gemm(c, rp, x, w_router, ws_split, partial, status, s);
   if (e != cudaSuccess) return e;
-  cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_sel);
+  if (sm_sel > 48 * 1024)
+    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_sel);
   select_kernel<<<grid, THREADS, sm_sel, s>>>(partial, rp.nsplit, rp.Epad, b_router, sel_bias,
                                               logits, topk_idx, topk_w, p);
   return cudaGetLastError();

@@ -299,8 +299,14 @@ cudaError_t launch_router_gemm(const Cfg& c, const RouterPlan& rp, const void* x
   uint32_t cols = 32;
   while ((int)cols < rp.n_acc * rp.acc_cols) cols <<= 1;
   p.tmem_cols = cols;
-  cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)SMEM_BYTES);
+  static bool attr_set[64];  // once per device, outside any stream capture
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)SMEM_BYTES);
+    attr_set[dev & 63] = true;
+  }
   const dim3 grid((c.N + BM - 1) / BM, rp.nsplit);
   router_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(mx, mw, p);
   return cudaGetLastError();

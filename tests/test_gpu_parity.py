@@ -225,6 +225,10 @@ EDGE = {
                                         num_ranks=2, score_fn=0, num_groups=1, topk_groups=1,
                                         capacity_factor=0.05, d_ff=32, shared_d_ff=0,
                                         sel_bias_std=0.0),
+    # few rows per expert: the token-major small-segment expert kernel, ragged sizes
+    "small_segments_ragged": small(tokens=40, hidden=264, num_experts=64, top_k=4, num_ranks=8,
+                                   num_groups=8, topk_groups=4, capacity_factor=1.0, d_ff=200,
+                                   shared_d_ff=72),
     "capacity_exact_boundary": small(tokens=256, hidden=64, num_experts=4, top_k=1, num_ranks=4,
                                      score_fn=0, num_groups=1, topk_groups=1,
                                      capacity_factor=1.0, d_ff=32, shared_d_ff=0,
@@ -261,3 +265,27 @@ def test_large_selection_bias_forces_choice_but_not_weights():
     idx = host(b.topk_idx)
     assert np.all(idx[:, 0:2] == [1, 2]) or np.all(np.sort(idx[:, :2], 1) == [1, 2])
     assert not np.any(idx == 9)
+
+
+def test_layer_replays_from_a_cuda_graph_bit_exactly():
+    """The five C-ABI calls can be captured in a CUDA graph; replay gives the same
+    bits as direct calls (the benchmark times graph replays)."""
+    from expert_routing_router_b300 import moe
+    for w in (EDGE["ragged_sigmoid_groups_shared"], W.DSV3_DECODE.with_tokens(8)):
+        inp = W.make_inputs(w, seed=2, device="cuda")
+        bias0 = inp["sel_bias"].clone()
+        b = moe.LayerBuffers(w)
+        moe.run_layer(b, inp, bias_step=w.bias_step)
+        torch.cuda.synchronize()
+        ref_out, ref_bias = b.out.clone(), inp["sel_bias"].clone()
+        inp["sel_bias"].copy_(bias0)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            moe.run_layer(b, inp, bias_step=w.bias_step)
+        inp["sel_bias"].copy_(bias0)
+        b.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(b.out, ref_out)
+        assert torch.equal(inp["sel_bias"], ref_bias)
+        assert int(b.workspace[:4].view(torch.int32).item()) == 0
