@@ -59,6 +59,23 @@ def workload(name):
     return w.with_tokens(int(n)) if n else w
 
 
+def measured_ffn_traffic():
+    """DRAM bytes per moe_expert_ffn call from the committed ncu launch list, if that
+    capture was taken on the current kernel source (else None)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "launches_dsv3_prefill.md")
+    srcs = [os.path.join(ROOT, "expert_routing_router_b300", "csrc", f)
+            for f in ("ffn_tc.cu", "tc_ptx.cuh")]
+    if not os.path.exists(prof):
+        return None
+    vals = dict(l.split(": ", 1) for l in open(prof).read().splitlines()
+                if l.startswith(("traffic_bytes_per_ffn_call:", "kernel_source_sha256_16:")))
+    h = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
+    if vals.get("kernel_source_sha256_16", "").strip() != h:
+        return None
+    return float(vals["traffic_bytes_per_ffn_call"])
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -339,7 +356,9 @@ def run_native(a, w, rank, world, local):
                      "bound": "tensor", "achieved": ffn_tflops, "peak": pk["bf16_sust"],
                      "unit": "TFLOP/s", "frac": ffn_tflops / pk["bf16_sust"],
                      "peak_kind": f"{pk['src']} sustained bf16 (kernel timed inside the step)",
-                     "frac_of_burst": ffn_tflops / pk["bf16"], "traffic": None,
+                     "frac_of_burst": ffn_tflops / pk["bf16"],
+                     "traffic": (measured_ffn_traffic() if w.name == "dsv3_prefill" else None),
+                     "traffic_unit": "bytes per moe_expert_ffn call (ncu dram read+write)",
                      "algorithmic_flops_per_launch": flops},
         "dispatch_combine": {"bytes": disp_b + comb_b, "achieved": dc_gbs, "unit": "GB/s",
                              "peak": pk["hbm"], "frac": dc_gbs / pk["hbm"],
