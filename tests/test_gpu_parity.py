@@ -184,6 +184,32 @@ def test_dsv3_prefill_and_bias_update(dsv3_inputs):
     inp["sel_bias"].copy_(bias0)
 
 
+def test_dsv3_prefill_graph_replay_matches_direct_calls(dsv3_inputs):
+    """Full-size layer in the launch form the benchmark times (CUDA graph replay):
+    bit-identical to direct C-ABI calls."""
+    from expert_routing_router_b300 import moe
+    w, (inp, _) = W.DSV3_PREFILL, dsv3_inputs
+    bias0 = inp["sel_bias"].clone()
+    b = moe.LayerBuffers(w)
+    moe.run_layer(b, inp, bias_step=w.bias_step)
+    torch.cuda.synchronize()
+    ref_out, ref_bias = b.out.clone(), inp["sel_bias"].clone()
+    inp["sel_bias"].copy_(bias0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.run_layer(b, inp, bias_step=w.bias_step)
+    inp["sel_bias"].copy_(bias0)
+    b.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(b.out, ref_out)
+    assert torch.equal(inp["sel_bias"], ref_bias)
+    assert int(b.workspace[:4].view(torch.int32).item()) == 0
+    inp["sel_bias"].copy_(bias0)
+    del b, g
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("T", W.DECODE_TOKENS)
 def test_dsv3_decode_sweep(dsv3_inputs, T):
     w = W.DSV3_DECODE.with_tokens(T)
