@@ -60,6 +60,7 @@ struct TcParams {
   __nv_bfloat16* out1;  // shared-expert output, indexed by token
   int* err;
   int E, n_shared, d, F, Fs;
+  int stall_cta;  // self-test only: this CTA arms its first ring slot without loading it
 };
 
 struct Ctl {
@@ -228,6 +229,16 @@ grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_consta
           uint8_t* sa = smem + (size_t)stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
+          if (blockIdx.x == p.stall_cta && t == (int)blockIdx.x && k0 == 0) {
+            // self-test: the slot's bytes never arrive, so the MMA's bounded wait runs out
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           tma_load(sa, ma, &ctl->full[stage], k0, ld.a_row);
           if (MODE == GATE_UP) {
             tma_load(sb, mb, &ctl->full[stage], k0, ld.b_row);
@@ -416,7 +427,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint3
 cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert_start,
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,
-                          void* yperm, void* yshared, void* h, int* status, cudaStream_t s) {
+                          void* yperm, void* yshared, void* h, int* status, cudaStream_t s,
+                          int stall_cta) {
   const bool sh = c.Fs > 0;
   __nv_bfloat16* h_routed = static_cast<__nv_bfloat16*>(h);
   __nv_bfloat16* h_shared = h_routed + (size_t)c.A * c.F;
@@ -429,7 +441,7 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
   if (sh && (!make_map(&a1, x, c.d, c.N, BM) || !make_map(&b1, shared_gate_up, c.d, 2 * c.Fs, BN / 2)))
     return cudaErrorInvalidValue;
   TcParams p{expert_start, kept_counts, h_routed, h_shared, status,
-             c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
+             c.E, sh ? c.N : 0, c.d, c.F, c.Fs, stall_cta};
   const int grid = num_sms();
   auto k1 = grouped_ffn_kernel<GATE_UP>;
   auto k2 = grouped_ffn_kernel<DOWN>;
@@ -453,6 +465,7 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
     return cudaErrorInvalidValue;
   p.out0 = static_cast<__nv_bfloat16*>(yperm);
   p.out1 = static_cast<__nv_bfloat16*>(yshared);
+  p.stall_cta = -1;  // only the first GEMM takes part in the self-test
   k2<<<grid, THREADS, SMEM_BYTES, s>>>(a0, a1, b0, b1, p);
   return cudaGetLastError();
 }

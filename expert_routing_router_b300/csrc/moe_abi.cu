@@ -127,6 +127,51 @@ moe_status ws_check(const Cfg& c, void* ws, size_t bytes, WsLayout* w) {
 
 moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// stall_cta >= 0 (self-test only) runs the prefill tensor-core kernels with that CTA's
+// first ring slot never loaded; otherwise the kernel is chosen by rows per expert.
+moe_status expert_ffn_impl(const moe_config* cfg, const void* xperm, const int32_t* expert_start,
+                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
+                           const void* x, const void* shared_gate_up, const void* shared_down,
+                           void* yperm, void* yshared, void* workspace, size_t workspace_bytes,
+                           void* stream, int stall_cta) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!xperm || !expert_start || !kept_counts || !w_gate_up || !w_down || !yperm)
+    return MOE_ERR_INVALID_ARG;
+  if (c.Fs > 0 && (!x || !shared_gate_up || !shared_down || !yshared)) return MOE_ERR_INVALID_ARG;
+  const void* acts[] = {xperm, w_gate_up, w_down, yperm};
+  for (const void* p : acts)
+    if (!aligned(p, 16)) return MOE_ERR_INVALID_ARG;
+  if (c.Fs > 0 && (!aligned(x, 16) || !aligned(shared_gate_up, 16) || !aligned(shared_down, 16) ||
+                   !aligned(yshared, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_start, 4) || !aligned(kept_counts, 4)) return MOE_ERR_INVALID_ARG;
+  WsLayout w;
+  if ((st = ws_check(c, workspace, workspace_bytes, &w)) != MOE_OK) return st;
+  if ((st = check_device()) != MOE_OK) return st;
+  void* h = static_cast<char*>(workspace) + w.h;
+  int* status = reinterpret_cast<int*>(static_cast<char*>(workspace) + w.status);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* xs = c.Fs > 0 ? x : nullptr;
+  if (stall_cta >= 0) {
+    if (c.act != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+    return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
+                                   shared_gate_up, shared_down, yperm, yshared, h, status, s,
+                                   stall_cta));
+  }
+  if (c.act == MOE_DTYPE_F32)
+    return from_cuda(launch_ffn_simt(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
+                                     shared_gate_up, shared_down, yperm, yshared, h, s));
+  // few rows per expert (decode): token-major kernel with right-sized token loads
+  if (c.A < (int64_t)kSmallRowsPerExpert * c.E)
+    return from_cuda(launch_ffn_tc_small(c, xperm, expert_start, kept_counts, w_gate_up, w_down,
+                                         xs, shared_gate_up, shared_down, yperm, yshared, h,
+                                         status, s));
+  return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
+                                 shared_gate_up, shared_down, yperm, yshared, h, status, s));
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -218,36 +263,20 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, const int32_
                           const void* x, const void* shared_gate_up, const void* shared_down,
                           void* yperm, void* yshared, void* workspace, size_t workspace_bytes,
                           void* stream) {
-  Cfg c;
-  moe_status st = make_cfg(cfg, &c);
-  if (st != MOE_OK) return st;
-  if (!xperm || !expert_start || !kept_counts || !w_gate_up || !w_down || !yperm)
-    return MOE_ERR_INVALID_ARG;
-  if (c.Fs > 0 && (!x || !shared_gate_up || !shared_down || !yshared)) return MOE_ERR_INVALID_ARG;
-  const void* acts[] = {xperm, w_gate_up, w_down, yperm};
-  for (const void* p : acts)
-    if (!aligned(p, 16)) return MOE_ERR_INVALID_ARG;
-  if (c.Fs > 0 && (!aligned(x, 16) || !aligned(shared_gate_up, 16) || !aligned(shared_down, 16) ||
-                   !aligned(yshared, 16)))
-    return MOE_ERR_INVALID_ARG;
-  if (!aligned(expert_start, 4) || !aligned(kept_counts, 4)) return MOE_ERR_INVALID_ARG;
-  WsLayout w;
-  if ((st = ws_check(c, workspace, workspace_bytes, &w)) != MOE_OK) return st;
-  if ((st = check_device()) != MOE_OK) return st;
-  void* h = static_cast<char*>(workspace) + w.h;
-  int* status = reinterpret_cast<int*>(static_cast<char*>(workspace) + w.status);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const void* xs = c.Fs > 0 ? x : nullptr;
-  if (c.act == MOE_DTYPE_F32)
-    return from_cuda(launch_ffn_simt(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
-                                     shared_gate_up, shared_down, yperm, yshared, h, s));
-  // few rows per expert (decode): token-major kernel with right-sized token loads
-  if (c.A < (int64_t)kSmallRowsPerExpert * c.E)
-    return from_cuda(launch_ffn_tc_small(c, xperm, expert_start, kept_counts, w_gate_up, w_down,
-                                         xs, shared_gate_up, shared_down, yperm, yshared, h,
-                                         status, s));
-  return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
-                                 shared_gate_up, shared_down, yperm, yshared, h, status, s));
+  return expert_ffn_impl(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
+                         shared_gate_up, shared_down, yperm, yshared, workspace, workspace_bytes,
+                         stream, -1);
+}
+
+moe_status moe_selftest_ffn_stall(const moe_config* cfg, const void* xperm,
+                                  const int32_t* expert_start, const int32_t* kept_counts,
+                                  const void* w_gate_up, const void* w_down, const void* x,
+                                  const void* shared_gate_up, const void* shared_down, void* yperm,
+                                  void* yshared, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  return expert_ffn_impl(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
+                         shared_gate_up, shared_down, yperm, yshared, workspace, workspace_bytes,
+                         stream, 0);
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* yperm, const int32_t* slot_of,

@@ -99,7 +99,8 @@ cudaError_t launch_ffn_simt(const Cfg& c, const void* xperm, const int32_t* expe
 cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert_start,
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,
-                          void* yperm, void* yshared, void* h, int* status, cudaStream_t s);
+                          void* yperm, void* yshared, void* h, int* status, cudaStream_t s,
+                          int stall_cta = -1);
 cudaError_t launch_ffn_tc_small(const Cfg& c, const void* xperm, const int32_t* expert_start,
                                 const int32_t* kept_counts, const void* w_gate_up,
                                 const void* w_down, const void* x, const void* shared_gate_up,

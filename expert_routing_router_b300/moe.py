@@ -35,7 +35,8 @@ class MoeError(RuntimeError):
 
 
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc",
-           "moe_expert_ffn", "moe_combine", "moe_bias_update", "moe_status_string")
+           "moe_expert_ffn", "moe_selftest_ffn_stall", "moe_combine", "moe_bias_update",
+           "moe_status_string")
 
 
 def _load():
@@ -50,6 +51,7 @@ def _load():
     lib.moe_dispatch.argtypes = [C] + [P] * 12 + [S, P]
     lib.moe_dispatch_noalloc.argtypes = [C] + [P] * 11 + [P]
     lib.moe_expert_ffn.argtypes = [C] + [P] * 11 + [S, P]
+    lib.moe_selftest_ffn_stall.argtypes = [C] + [P] * 11 + [S, P]
     lib.moe_combine.argtypes = [C] + [P] * 6 + [P]
     lib.moe_bias_update.argtypes = [C, P, P, F, P]
     lib.moe_status_string.argtypes = [I]
@@ -130,6 +132,16 @@ def moe_dispatch_noalloc(cfg, topk_idx, x, xperm, expert_counts, kept_counts, ex
 def moe_expert_ffn(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x, shared_gate_up,
                    shared_down, yperm, yshared, workspace, stream=None):
     _check("moe_expert_ffn", _lib.moe_expert_ffn(
+        ctypes.byref(cfg), _p(xperm), _p(expert_start), _p(kept_counts), _p(w_gate_up),
+        _p(w_down), _p(x), _p(shared_gate_up), _p(shared_down), _p(yperm), _p(yshared),
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_selftest_ffn_stall(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
+                           shared_gate_up, shared_down, yperm, yshared, workspace, stream=None):
+    """Failure-handling self-test: the prefill expert kernels with one pipeline slot never
+    loaded (outputs invalid; the workspace status word becomes nonzero)."""
+    _check("moe_selftest_ffn_stall", _lib.moe_selftest_ffn_stall(
         ctypes.byref(cfg), _p(xperm), _p(expert_start), _p(kept_counts), _p(w_gate_up),
         _p(w_down), _p(x), _p(shared_gate_up), _p(shared_down), _p(yperm), _p(yshared),
         _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -191,6 +191,21 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xperm, cons
                           void* yperm, void* yshared, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* Self-test of the device-side failure handling (the pages have no counterpart).
+ * Same arguments and validation as moe_expert_ffn with bf16 activations, but it
+ * always runs the prefill tensor-core kernels and makes CTA 0 of the first GEMM arm
+ * one pipeline slot whose data is never loaded.  That CTA's bounded wait (about 2 s)
+ * runs out, it records a nonzero code in the workspace status word, waits (bounded)
+ * for its own copies and MMAs, frees its tensor memory and exits; every other CTA
+ * completes normally and the CUDA context stays usable.  Outputs are invalid.
+ * Returns MOE_ERR_UNSUPPORTED for fp32 layers. */
+MOE_API moe_status moe_selftest_ffn_stall(const moe_config* cfg, const void* xperm,
+                                          const int32_t* expert_start, const int32_t* kept_counts,
+                                          const void* w_gate_up, const void* w_down,
+                                          const void* x, const void* shared_gate_up,
+                                          const void* shared_down, void* yperm, void* yshared,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Combine.  Same page, step 4 (outputs return to token order, weighted by the router
  * scores and summed); section "Load balancing and capacity" (a skipped token passes
  * through the residual connection unchanged).
