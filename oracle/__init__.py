@@ -38,6 +38,7 @@ def _lib():
         lib.oracle_router_logits.argtypes = [I, I, I, I, P, P, P, P]
         lib.oracle_route.argtypes = [I, I, I, I, I, I, I, P, P, P, P]
         lib.oracle_dispatch.argtypes = [I, I, I, I, I, F, P, P, P, P, P, P, P, P, P]
+        lib.oracle_dispatch_mode.argtypes = [I, I, I, I, I, F, I, P, P, P, P, P, P, P, P, P]
         lib.oracle_expert_rows.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P]
         lib.oracle_combine.argtypes = [I, P, I, I, I, P, P, P, P, P, P]
         lib.oracle_layer_tokens.argtypes = [I, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P]
@@ -104,24 +105,30 @@ def route(logits, k, score_fn=0, normalize=True, num_groups=1, topk_groups=1, se
     return idx, w
 
 
-def dispatch(idx, E, R, rank_map=0, cf=0.0):
+def dispatch(idx, E, R, rank_map=0, cf=0.0, mode=0):
+    """Counting, capacity and send order.  mode 0: packed, token-order priority;
+    mode 1: capacity-padded [E, C] slots, choice-major priority (needs cf > 0)."""
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     N, k = idx.shape
     A = N * k
+    C = capacity(N, k, E, cf)
+    rows = A if mode == 0 else E * C
     out = dict(
         expert_counts=np.empty(E, np.int32), kept_counts=np.empty(E, np.int32),
         expert_start=np.empty(E, np.int32), rank_counts=np.empty(R, np.int32),
         rank_offsets=np.empty(R + 1, np.int32), slot_of=np.empty(A, np.int32),
-        perm_src=np.empty(A, np.int32), num_kept=np.empty(1, np.int32))
-    rc = _lib().oracle_dispatch(N, E, k, R, rank_map, float(cf), _p(idx),
-                                *[_p(out[n]) for n in ("expert_counts", "kept_counts",
-                                                       "expert_start", "rank_counts",
-                                                       "rank_offsets", "slot_of", "perm_src",
-                                                       "num_kept")])
+        perm_src=np.empty(max(rows, 1), np.int32), num_kept=np.empty(1, np.int32))
+    rc = _lib().oracle_dispatch_mode(N, E, k, R, rank_map, float(cf), int(mode), _p(idx),
+                                     *[_p(out[n]) for n in ("expert_counts", "kept_counts",
+                                                            "expert_start", "rank_counts",
+                                                            "rank_offsets", "slot_of", "perm_src",
+                                                            "num_kept")])
     if rc != 0:
         raise ValueError(f"oracle_dispatch rejected the arguments (rc={rc})")
+    out["perm_src"] = out["perm_src"][:rows]
     out["num_kept"] = int(out["num_kept"][0])
-    out["capacity"] = capacity(N, k, E, cf)
+    out["capacity"] = C
+    out["send_rows"] = rows
     return out
 
 

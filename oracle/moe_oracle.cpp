@@ -324,18 +324,30 @@ int oracle_route(int N, int E, int k, int score_fn, int normalize, int num_group
 //   slot_of       [N*k] slot of assignment a = t*k + j, or -1 if dropped
 //   perm_src      [N*k] perm_src[slot] = a for slot < num_kept, -1 beyond
 //   num_kept      [1]
-int oracle_dispatch(int N, int E, int k, int R, int rank_map, float cf, const int32_t* idx,
-                    int32_t* expert_counts, int32_t* kept_counts, int32_t* expert_start,
-                    int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
-                    int32_t* perm_src, int32_t* num_kept) {
+//
+// mode 0 (packed): assignments compete for capacity in token order (t, then j), and
+//   the send buffer is packed: expert segments follow each other with no gaps.
+// mode 1 (capacity-padded, choice-major): the buffer reserves C rows per expert, as
+//   [BZ] exercise 2 describes ("each expert's buffer is reserved at the mean times
+//   1.25"), so expert e's rows start at (its send position) * C; capacity goes to all
+//   first choices in token order, then all second choices, and so on (the priority
+//   GShard uses).  Padding rows carry perm_src = -1.  Requires cf > 0.  perm_src then
+//   spans E*C rows; rank_offsets are the padded rank starts.
+int oracle_dispatch_mode(int N, int E, int k, int R, int rank_map, float cf, int mode,
+                         const int32_t* idx, int32_t* expert_counts, int32_t* kept_counts,
+                         int32_t* expert_start, int32_t* rank_counts, int32_t* rank_offsets,
+                         int32_t* slot_of, int32_t* perm_src, int32_t* num_kept) {
   if (R < 1 || R > E) return -1;
   if (rank_map == 0 && E % R != 0) return -1;
+  if (mode != 0 && mode != 1) return -1;
+  if (mode == 1 && !(cf > 0.0f)) return -1;
   const int64_t A = static_cast<int64_t>(N) * k;
   const int C = oracle_capacity(N, k, E, cf);
   std::vector<int64_t> seen(E, 0);
   std::vector<int64_t> pos(A);
   for (int e = 0; e < E; ++e) expert_counts[e] = 0;
-  for (int64_t a = 0; a < A; ++a) {  // token order: t major, choice j minor
+  for (int64_t p = 0; p < A; ++p) {  // priority order
+    const int64_t a = (mode == 0) ? p : (p % N) * k + p / N;  // mode 1: j major, t minor
     const int e = idx[a];
     if (e < 0 || e >= E) return -2;
     pos[a] = seen[e]++;
@@ -348,18 +360,22 @@ int oracle_dispatch(int N, int E, int k, int R, int rank_map, float cf, const in
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
     return rank_of(a, E, R, rank_map) < rank_of(b, E, R, rank_map);
   });
-  int64_t run = 0;
+  int64_t run = 0, kept_total = 0;
   for (int r = 0; r < R; ++r) rank_counts[r] = 0;
+  for (int r = 0; r <= R; ++r) rank_offsets[r] = -1;
   for (int i = 0; i < E; ++i) {
     const int e = order[i];
+    const int r = rank_of(e, E, R, rank_map);
+    if (rank_offsets[r] < 0) rank_offsets[r] = static_cast<int32_t>(run);
     expert_start[e] = static_cast<int32_t>(run);
-    run += kept_counts[e];
-    rank_counts[rank_of(e, E, R, rank_map)] += kept_counts[e];
+    run += (mode == 0) ? kept_counts[e] : C;
+    kept_total += kept_counts[e];
+    rank_counts[r] += kept_counts[e];
   }
-  rank_offsets[0] = 0;
-  for (int r = 0; r < R; ++r) rank_offsets[r + 1] = rank_offsets[r] + rank_counts[r];
-  *num_kept = static_cast<int32_t>(run);
-  for (int64_t a = 0; a < A; ++a) perm_src[a] = -1;
+  rank_offsets[R] = static_cast<int32_t>(run);
+  *num_kept = static_cast<int32_t>(kept_total);
+  const int64_t rows = (mode == 0) ? A : static_cast<int64_t>(E) * C;
+  for (int64_t s = 0; s < rows; ++s) perm_src[s] = -1;
   for (int64_t a = 0; a < A; ++a) {
     const int e = idx[a];
     if (pos[a] < C) {
@@ -371,6 +387,15 @@ int oracle_dispatch(int N, int E, int k, int R, int rank_map, float cf, const in
     }
   }
   return 0;
+}
+
+int oracle_dispatch(int N, int E, int k, int R, int rank_map, float cf, const int32_t* idx,
+                    int32_t* expert_counts, int32_t* kept_counts, int32_t* expert_start,
+                    int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
+                    int32_t* perm_src, int32_t* num_kept) {
+  return oracle_dispatch_mode(N, E, k, R, rank_map, cf, 0, idx, expert_counts, kept_counts,
+                              expert_start, rank_counts, rank_offsets, slot_of, perm_src,
+                              num_kept);
 }
 
 // ---------------------------------------------------------------- 6. expert FFN

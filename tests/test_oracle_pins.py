@@ -389,3 +389,66 @@ def test_bias_update_sign_rule():
     # fractional mean (N*k/E = 2.5): 3 is above, 2 below
     b2 = oracle.bias_update(np.array([3, 2, 2, 3], np.int32), np.zeros(4, np.float32), 5, 2, 0.5)
     assert b2.tolist() == [-0.5, 0.5, 0.5, -0.5]
+
+
+# ------------------------------------------------------------------ capacity-padded, choice-major
+
+def test_choice_major_priority_worked_example():
+    """3 tokens, 2 experts, top-2, C = 2.  Token order drops token 2's first choice
+    (expert 1 is full with tokens 0 and 1's second choices); choice-major priority
+    (all first choices first) keeps it and drops token 1's second choice instead."""
+    idx = np.array([[0, 1], [0, 1], [1, 0]], np.int32)
+    cf = 0.6                                        # C = ceil(0.6 * 3 * 2 / 2) = 2
+    d0 = oracle.dispatch(idx, 2, 1, 0, cf, mode=0)
+    d1 = oracle.dispatch(idx, 2, 1, 0, cf, mode=1)
+    assert d0["capacity"] == d1["capacity"] == 2
+    assert (d0["slot_of"].reshape(3, 2) >= 0).tolist() == [[True, True], [True, True],
+                                                          [False, False]]
+    assert (d1["slot_of"].reshape(3, 2) >= 0).tolist() == [[True, True], [True, False],
+                                                          [True, False]]
+    # padded layout: expert e's rows start at e * C; token 2's first choice is row 0 of
+    # expert 1 (it came first in priority order), token 0's second choice row 1
+    assert d1["expert_start"].tolist() == [0, 2]
+    assert d1["slot_of"].tolist() == [0, 3, 1, -1, 2, -1]
+    assert d1["perm_src"].tolist() == [0, 2, 4, 1]
+
+
+@pytest.mark.parametrize("N,E,k,R,rank_map,cf", [
+    (40, 4, 2, 2, 0, 1.0), (37, 8, 3, 4, 0, 0.7), (50, 6, 2, 3, 1, 1.25), (64, 16, 4, 5, 1, 0.5)])
+def test_choice_major_padded_dispatch_bruteforce(N, E, k, R, rank_map, cf):
+    rng = np.random.default_rng(N * 7 + E)
+    p = rng.dirichlet(np.ones(E) * 0.5)
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(N)]).astype(np.int32)
+    d = oracle.dispatch(idx, E, R, rank_map, cf, mode=1)
+    C = d["capacity"]
+    flat = idx.reshape(-1)
+    order = [t * k + j for j in range(k) for t in range(N)]   # choice-major priority
+    rank_in = {}
+    kept = np.zeros(N * k, bool)
+    pos = np.zeros(N * k, int)
+    for a in order:
+        e = flat[a]
+        before = rank_in.get(e, 0)
+        pos[a] = before
+        kept[a] = before < C
+        rank_in[e] = before + 1
+    np.testing.assert_array_equal(d["expert_counts"], np.bincount(flat, minlength=E))
+    np.testing.assert_array_equal(d["kept_counts"], np.minimum(d["expert_counts"], C))
+    np.testing.assert_array_equal(d["slot_of"] >= 0, kept)
+    ranks = np.array([(e % R) if rank_map else e // (E // R) for e in range(E)])
+    send = sorted(range(E), key=lambda e: (ranks[e], e))
+    for sp, e in enumerate(send):
+        assert d["expert_start"][e] == sp * C
+    for a in np.nonzero(kept)[0]:
+        assert d["slot_of"][a] == d["expert_start"][flat[a]] + pos[a]
+    assert d["send_rows"] == E * C and d["perm_src"].size == E * C
+    for s in range(E * C):
+        a = d["perm_src"][s]
+        if a >= 0:
+            assert d["slot_of"][a] == s
+    assert (d["perm_src"] >= 0).sum() == kept.sum() == d["num_kept"]
+    first = [send.index(e) for e in range(E)]
+    for r in range(R):
+        assert d["rank_counts"][r] == d["kept_counts"][ranks == r].sum()
+        assert d["rank_offsets"][r] == min(first[e] for e in range(E) if ranks[e] == r) * C
+    assert d["rank_offsets"][R] == E * C
