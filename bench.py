@@ -131,7 +131,7 @@ class Clocks:
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                       "-lms", "200", "-i", str(index)], stdout=self.f,
+                                       "-lms", "50", "-i", str(index)], stdout=self.f,
                                       stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
@@ -289,7 +289,6 @@ def run_native(a, w, rank, world, local):
         evs[i][1].record(s)
     torch.cuda.synchronize()
     barrier(world)
-    clocks = clk.stop() if clk else None
     step_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
     total_s = max_over_ranks(step_ms.sum() / 1e3, world)
     value = weak_scaling_value(w.tokens, a.steps, world, total_s)
@@ -375,6 +374,7 @@ def run_native(a, w, rank, world, local):
     torch.cuda.synchronize()
     torch.cuda.set_stream(torch.cuda.default_stream(dev))
     barrier(world)
+    clocks = clk.stop() if clk else None  # sampled over the timed, per-stage and e2e loops
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e_value = weak_scaling_value(w.tokens, a.steps, world, e2e_s)
     if bias0 is not None:

@@ -9,7 +9,8 @@
 // Single-GPU form: the "send buffer" xperm holds the kept rows in the order an
 // all-to-all would send them (rank, then expert, then token order), and the
 // per-rank counts/offsets are its split sizes.  Deterministic, no inter-CTA waits:
-//   K2a count   one CTA per chunk of kChunk assignments: per-chunk histogram
+//   K2a count   one CTA per chunk of kChunk assignments (in priority order): per-chunk
+//               histogram; the capacity-padded layout also clears perm_src here
 //   K2b scan    one CTA: per-expert prefix over chunks (chunk bases), routed counts,
 //               kept = min(count, C), send-order expert starts, rank counts/offsets
 //   K2c assign  one CTA per chunk: stable (token-order) rank of each assignment
@@ -25,17 +26,31 @@ namespace {
 
 constexpr int T2 = 256;  // threads of the count / scan / assign kernels
 
+// Assignments compete for capacity in priority order p = 0..A-1.  Packed: p is the
+// assignment index a = t*k + j (token order).  Capacity-padded: p = j*N + t, every
+// token's first choice before any second choice (choice-major).
+__device__ __forceinline__ int64_t assignment_of(int64_t p, int N, int k, int mode) {
+  return mode == MOE_DISPATCH_CAPACITY_PADDED ? (p % N) * k + p / N : p;
+}
+
 __global__ void __launch_bounds__(T2)
-count_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int32_t* __restrict__ chunk_hist) {
+count_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, int mode,
+             int32_t* __restrict__ chunk_hist, int32_t* __restrict__ perm_src, int64_t send_rows) {
   __shared__ int hist[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += T2) hist[e] = 0;
   __syncthreads();
-  const int64_t a0 = (int64_t)blockIdx.x * kChunk;
-  const int64_t a1 = min(a0 + kChunk, A);
-  for (int64_t a = a0 + threadIdx.x; a < a1; a += T2) {
-    const int e = idx[a];
+  const int64_t p0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t p1 = min(p0 + kChunk, A);
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += T2) {
+    const int e = idx[assignment_of(p, N, k, mode)];
     if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);
   }
+  // padded layout: rows without an assignment hold -1 (the assign kernel, which runs
+  // after this one, overwrites the kept rows)
+  if (mode == MOE_DISPATCH_CAPACITY_PADDED)
+    for (int64_t r = (int64_t)blockIdx.x * T2 + threadIdx.x; r < send_rows;
+         r += (int64_t)gridDim.x * T2)
+      perm_src[r] = -1;
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += T2) chunk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
 }
@@ -52,6 +67,7 @@ __device__ __forceinline__ int send_pos(int e, int E, int R, int rank_map) {
 
 __global__ void __launch_bounds__(T2)
 scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int R, int rank_map, int C,
+            int mode,
             int32_t* __restrict__ expert_counts, int32_t* __restrict__ kept_counts,
             int32_t* __restrict__ expert_start, int32_t* __restrict__ rank_counts,
             int32_t* __restrict__ rank_offsets, int32_t* __restrict__ num_kept) {
@@ -90,7 +106,8 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int R, int ra
   if (threadIdx.x < E) start_by_pos[threadIdx.x] = base + incl - v;
   if (threadIdx.x == E - 1) start_by_pos[E] = base + incl;
   __syncthreads();
-  if (e < E) expert_start[e] = start_by_pos[pos];
+  const bool padded = mode == MOE_DISPATCH_CAPACITY_PADDED;  // expert rows start at pos * C
+  if (e < E) expert_start[e] = padded ? pos * C : start_by_pos[pos];
   // ranks: send positions of rank r are [P_r, P_{r+1})
   for (int r = threadIdx.x; r < R; r += T2) {
     int p0, p1;
@@ -102,15 +119,15 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int R, int ra
       p0 = r * (E / R);
       p1 = p0 + E / R;
     }
-    rank_offsets[r] = start_by_pos[p0];
+    rank_offsets[r] = padded ? p0 * C : start_by_pos[p0];
     rank_counts[r] = start_by_pos[p1] - start_by_pos[p0];
-    if (r == R - 1) rank_offsets[R] = start_by_pos[p1];
+    if (r == R - 1) rank_offsets[R] = padded ? p1 * C : start_by_pos[p1];
   }
   if (threadIdx.x == 0) *num_kept = start_by_pos[E];
 }
 
 __global__ void __launch_bounds__(T2)
-assign_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int C,
+assign_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, int C, int mode,
               const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ expert_start,
               const int32_t* __restrict__ num_kept, int32_t* __restrict__ slot_of,
               int32_t* __restrict__ perm_src) {
@@ -123,10 +140,11 @@ assign_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int C,
   for (int64_t a = a0; a < a1; a += T2) {
     for (int q = tid; q < (T2 / 32) * E; q += T2) wcnt[q / E][q % E] = 0;
     __syncthreads();  // also orders run[] updates of the previous round
-    const int64_t my = a + tid;
+    const int64_t my = a + tid;  // priority index of this thread's assignment
+    const int64_t asg = assignment_of(my, N, k, mode);
     int e = -1;
     if (my < a1) {
-      e = idx[my];
+      e = idx[asg];
       if ((unsigned)e >= (unsigned)E) e = -1;
     }
     const int key = (e >= 0) ? e : -1 - lane;  // invalid lanes never group together
@@ -148,18 +166,20 @@ assign_kernel(const int32_t* __restrict__ idx, int64_t A, int E, int C,
     if (my < a1) {
       if (e >= 0 && pos < C) {
         const int slot = expert_start[e] + pos;
-        slot_of[my] = slot;
-        perm_src[slot] = (int32_t)my;
+        slot_of[asg] = slot;
+        perm_src[slot] = (int32_t)asg;
       } else {
-        slot_of[my] = -1;
+        slot_of[asg] = -1;
       }
     }
     __syncthreads();  // wcnt is cleared at the top of the next round
   }
-  // rows past num_kept carry no assignment
-  const int nk = *num_kept;
-  for (int64_t s = a0 + tid; s < a1; s += T2)
-    if (s >= nk) perm_src[s] = -1;
+  // packed layout: rows past num_kept carry no assignment
+  if (mode == MOE_DISPATCH_PACKED) {
+    const int nk = *num_kept;
+    for (int64_t s = a0 + tid; s < a1; s += T2)
+      if (s >= nk) perm_src[s] = -1;
+  }
 }
 
 // K3: one CTA walks tokens; each 16-byte vector of a row is loaded once and stored
@@ -202,11 +222,13 @@ cudaError_t launch_dispatch(const Cfg& c, const int32_t* topk_idx, const void* x
                             int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
                             int32_t* perm_src, int32_t* num_kept, int32_t* chunk_hist,
                             cudaStream_t s) {
-  count_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.E, chunk_hist);
-  scan_kernel<<<1, T2, 0, s>>>(chunk_hist, c.n_chunks, c.E, c.R, c.rank_map, c.C, expert_counts,
-                               kept_counts, expert_start, rank_counts, rank_offsets, num_kept);
-  assign_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.E, c.C, chunk_hist, expert_start,
-                                          num_kept, slot_of, perm_src);
+  count_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.N, c.k, c.E, c.mode, chunk_hist,
+                                         perm_src, c.send_rows);
+  scan_kernel<<<1, T2, 0, s>>>(chunk_hist, c.n_chunks, c.E, c.R, c.rank_map, c.C, c.mode,
+                               expert_counts, kept_counts, expert_start, rank_counts,
+                               rank_offsets, num_kept);
+  assign_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.N, c.k, c.E, c.C, c.mode, chunk_hist,
+                                          expert_start, num_kept, slot_of, perm_src);
   if (xperm) {
     const int nvec = (int)((int64_t)c.d * c.act_bytes / 16);
     int grid = num_sms() * 8;

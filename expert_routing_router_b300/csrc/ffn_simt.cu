@@ -213,7 +213,7 @@ cudaError_t run(const Cfg& c, const void* xperm, const int32_t* expert_start,
   const int n_shared = c.Fs > 0 ? c.N : 0;
   // worst case: every segment adds at most one partial tile
   const int64_t max_tiles = c.A / BM + c.E + (n_shared + BM - 1) / BM + 1;
-  const int64_t h_shared_off = c.A * (int64_t)c.F;
+  const int64_t h_shared_off = c.send_rows * (int64_t)c.F;
   const int fmax = c.F > c.Fs ? c.F : c.Fs;
   dim3 g1((fmax + BN - 1) / BN, (unsigned)max_tiles);
   ffn_gate_up_kernel<T><<<g1, TS, 0, s>>>(

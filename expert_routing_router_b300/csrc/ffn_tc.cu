@@ -431,10 +431,10 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
                           int stall_cta) {
   const bool sh = c.Fs > 0;
   __nv_bfloat16* h_routed = static_cast<__nv_bfloat16*>(h);
-  __nv_bfloat16* h_shared = h_routed + (size_t)c.A * c.F;
+  __nv_bfloat16* h_shared = h_routed + (size_t)c.send_rows * c.F;
   CUtensorMap a0, a1, b0, b1;
   // G1: A = send buffer [A, d] / tokens [N, d]; B = [E*2F, d] / [2Fs, d]
-  if (!make_map(&a0, xperm, c.d, c.A, BM) || !make_map(&b0, w_gate_up, c.d, (uint64_t)c.E * 2 * c.F, BN / 2))
+  if (!make_map(&a0, xperm, c.d, c.send_rows, BM) || !make_map(&b0, w_gate_up, c.d, (uint64_t)c.E * 2 * c.F, BN / 2))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
@@ -457,7 +457,7 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // G2: A = h [A, F] / [N, Fs]; B = [E*d, F] / [d, Fs]
-  if (!make_map(&a0, h_routed, c.F, c.A, BM) || !make_map(&b0, w_down, c.F, (uint64_t)c.E * c.d, BN))
+  if (!make_map(&a0, h_routed, c.F, c.send_rows, BM) || !make_map(&b0, w_down, c.F, (uint64_t)c.E * c.d, BN))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;

@@ -444,11 +444,11 @@ cudaError_t launch_ffn_tc_small(const Cfg& c, const void* xperm, const int32_t* 
                           void* yperm, void* yshared, void* h, int* status, cudaStream_t s) {
   const bool sh = c.Fs > 0;
   __nv_bfloat16* h_routed = static_cast<__nv_bfloat16*>(h);
-  __nv_bfloat16* h_shared = h_routed + (size_t)c.A * c.F;
+  __nv_bfloat16* h_shared = h_routed + (size_t)c.send_rows * c.F;
   CUtensorMap w0, w1, x0, x1;
   // G1: weights [E*2F, d] / [2Fs, d] in 64-row boxes; tokens [A, d] / [N, d]
   if (!make_map(&w0, w_gate_up, c.d, (uint64_t)c.E * 2 * c.F, BW / 2) ||
-      !make_map(&x0, xperm, c.d, c.A, PIECE))
+      !make_map(&x0, xperm, c.d, c.send_rows, PIECE))
     return cudaErrorInvalidValue;
   w1 = w0;
   x1 = x0;
@@ -461,7 +461,7 @@ cudaError_t launch_ffn_tc_small(const Cfg& c, const void* xperm, const int32_t* 
   if (e != cudaSuccess) return e;
   // G2: weights [E*d, F] / [d, Fs] in 128-row boxes; tokens = h [A, F] / [N, Fs]
   if (!make_map(&w0, w_down, c.F, (uint64_t)c.E * c.d, BW) ||
-      !make_map(&x0, h_routed, c.F, c.A, PIECE))
+      !make_map(&x0, h_routed, c.F, c.send_rows, PIECE))
     return cudaErrorInvalidValue;
   w1 = w0;
   x1 = x0;

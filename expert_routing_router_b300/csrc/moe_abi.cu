@@ -63,6 +63,10 @@ moe_status make_cfg(const moe_config* in, Cfg* c) {
   if (m.d_ff < 8 || m.d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
   if (m.shared_d_ff < 0 || m.shared_d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
   if (m.act_dtype != MOE_DTYPE_F32 && m.act_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (m.dispatch_mode != MOE_DISPATCH_PACKED && m.dispatch_mode != MOE_DISPATCH_CAPACITY_PADDED)
+    return MOE_ERR_INVALID_ARG;
+  if (m.dispatch_mode == MOE_DISPATCH_CAPACITY_PADDED && !(m.capacity_factor > 0.0f))
+    return MOE_ERR_INVALID_ARG;
   const int64_t A = (int64_t)m.tokens * m.top_k;
   if (A > INT32_MAX / 2) return MOE_ERR_INVALID_ARG;  // slots are int32
   c->N = m.tokens;
@@ -90,6 +94,12 @@ moe_status make_cfg(const moe_config* in, Cfg* c) {
   } else {
     c->C = INT32_MAX;
   }
+  c->mode = m.dispatch_mode;
+  c->send_rows = A;
+  if (c->mode == MOE_DISPATCH_CAPACITY_PADDED) {
+    c->send_rows = (int64_t)c->C * m.num_experts;
+    if (c->send_rows > INT32_MAX / 2) return MOE_ERR_INVALID_ARG;  // slots are int32
+  }
   return MOE_OK;
 }
 
@@ -111,7 +121,7 @@ WsLayout layout(const Cfg& c) {
   w.chunk_hist = off;
   off += round_up((size_t)c.n_chunks * c.E * sizeof(int32_t));
   w.h = off;
-  off += round_up(((size_t)c.A * c.F + (size_t)c.N * c.Fs) * c.act_bytes);
+  off += round_up(((size_t)c.send_rows * c.F + (size_t)c.N * c.Fs) * c.act_bytes);
   w.sched = off;
   off += round_up(16 * 1024);
   w.total = off;
@@ -178,6 +188,15 @@ moe_status expert_ffn_impl(const moe_config* cfg, const void* xperm, const int32
 using namespace moe;
 
 extern "C" {
+
+moe_status moe_send_rows(const moe_config* cfg, int64_t* rows) {
+  Cfg c;
+  const moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!rows) return MOE_ERR_INVALID_ARG;
+  *rows = c.send_rows;
+  return MOE_OK;
+}
 
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
   Cfg c;

@@ -24,6 +24,8 @@ struct Cfg {
   int C;           // capacity (INT32 max = none)
   int n_chunks;    // ceil(A / kChunk)
   int act_bytes;   // 4 (fp32) or 2 (bf16)
+  int mode;        // MOE_DISPATCH_PACKED or MOE_DISPATCH_CAPACITY_PADDED
+  int64_t send_rows;  // rows of the send buffer: A (packed) or E * C (padded)
 };
 
 // Tensor-core router: padded sizes and the K slicing of its GEMM.

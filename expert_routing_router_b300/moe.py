@@ -25,7 +25,8 @@ class moe_config(ctypes.Structure):
                 ("score_fn", ctypes.c_int32), ("normalize_topk", ctypes.c_int32),
                 ("num_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("d_ff", ctypes.c_int32),
-                ("shared_d_ff", ctypes.c_int32), ("act_dtype", ctypes.c_int32)]
+                ("shared_d_ff", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
+                ("dispatch_mode", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -34,7 +35,7 @@ class MoeError(RuntimeError):
         super().__init__(f"{fn} failed: {status_string(status)}")
 
 
-EXPORTS = ("moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc",
+EXPORTS = ("moe_send_rows", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc",
            "moe_expert_ffn", "moe_selftest_ffn_stall", "moe_combine", "moe_bias_update",
            "moe_status_string")
 
@@ -47,6 +48,7 @@ def _load():
     P, S, I, F = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
     C = ctypes.POINTER(moe_config)
     lib.moe_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_send_rows.argtypes = [C, ctypes.POINTER(ctypes.c_int64)]
     lib.moe_route.argtypes = [C] + [P] * 8 + [S, P]
     lib.moe_dispatch.argtypes = [C] + [P] * 12 + [S, P]
     lib.moe_dispatch_noalloc.argtypes = [C] + [P] * 11 + [P]
@@ -74,7 +76,8 @@ def config(w):
     return moe_config(w.tokens, w.hidden, w.num_experts, w.top_k, w.num_ranks, w.rank_map,
                       w.score_fn, int(bool(w.normalize_topk)), w.num_groups, w.topk_groups,
                       float(w.capacity_factor), w.d_ff, w.shared_d_ff,
-                      DTYPE_F32 if w.act_dtype == "f32" else DTYPE_BF16)
+                      DTYPE_F32 if w.act_dtype == "f32" else DTYPE_BF16,
+                      int(getattr(w, "dispatch_mode", 0)))
 
 
 def _p(t):
@@ -94,6 +97,12 @@ def _stream(stream):
 def _check(fn, status):
     if status != MOE_OK:
         raise MoeError(fn, status)
+
+
+def moe_send_rows(cfg):
+    n = ctypes.c_int64(0)
+    _check("moe_send_rows", _lib.moe_send_rows(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
 
 
 def moe_workspace_size(cfg):
@@ -159,18 +168,20 @@ def moe_bias_update(cfg, expert_counts, sel_bias, step, stream=None):
 
 
 class LayerBuffers:
-    """Device buffers of one layer call, sized for the worst case (N*k kept rows)."""
+    """Device buffers of one layer call, sized for the worst case (every assignment
+    kept; the capacity-padded layout has E*C send rows)."""
 
     def __init__(self, w, device="cuda"):
         N, d, E, k, R = w.tokens, w.hidden, w.num_experts, w.top_k, w.num_ranks
         dt = w.torch_dtype
         i32 = dict(dtype=torch.int32, device=device)
         self.cfg = config(w)
+        S = moe_send_rows(self.cfg)
         self.logits = torch.empty(N, E, dtype=torch.float32, device=device)
         self.topk_idx = torch.empty(N, k, **i32)
         self.topk_w = torch.empty(N, k, dtype=torch.float32, device=device)
-        self.xperm = torch.empty(N * k, d, dtype=dt, device=device)
-        self.yperm = torch.empty(N * k, d, dtype=dt, device=device)
+        self.xperm = torch.empty(S, d, dtype=dt, device=device)
+        self.yperm = torch.empty(S, d, dtype=dt, device=device)
         self.yshared = torch.empty(N, d, dtype=dt, device=device) if w.shared_d_ff else None
         self.out = torch.empty(N, d, dtype=dt, device=device)
         self.expert_counts = torch.empty(E, **i32)
@@ -179,7 +190,7 @@ class LayerBuffers:
         self.rank_counts = torch.empty(R, **i32)
         self.rank_offsets = torch.empty(R + 1, **i32)
         self.slot_of = torch.empty(N * k, **i32)
-        self.perm_src = torch.empty(N * k, **i32)
+        self.perm_src = torch.empty(S, **i32)
         self.num_kept = torch.empty(1, **i32)
         nbytes = moe_workspace_size(self.cfg)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)

@@ -18,6 +18,8 @@ Workloads (named by what they are):
                       64 ranks, bias update step 1e-3.
   dsv3_decode         the same layer at 1, 8, 64, 128, 512 tokens, 40 ranks
                       assigned round-robin.
+  gshard_top2_padded  the GShard-shaped layer with the capacity-padded [E, C] send
+                      buffer and choice-major capacity priority.
 """
 from dataclasses import dataclass, replace
 import math
@@ -51,6 +53,7 @@ class Workload:
     sel_bias_std: float       # selection-only bias (sigmoid scoring)
     bias_step: float          # bias-update step (0 = no update in the step)
     expert_std: float = 0.02
+    dispatch_mode: int = 0    # 0 packed token-order capacity, 1 capacity-padded choice-major
 
     def with_tokens(self, n):
         return replace(self, tokens=n, name=f"{self.name.split('@')[0]}@{n}")
@@ -66,14 +69,15 @@ SWITCH_TOP1 = Workload("switch_top1_bf16", 16384, 1024, 32, 1, 8, RANK_CONTIGUOU
                        False, 1, 1, 1.25, 2048, 0, "bf16", 0.0, 0.0, 0.0)
 GSHARD_TOP2 = Workload("gshard_top2_skewed", 32768, 2048, 64, 2, 16, RANK_CONTIGUOUS,
                        SCORE_SOFTMAX, False, 1, 1, 1.25, 1408, 0, "bf16", 1.5, 0.0, 0.0)
+GSHARD_TOP2_PADDED = replace(GSHARD_TOP2, name="gshard_top2_padded", dispatch_mode=1)
 DSV3_PREFILL = Workload("dsv3_prefill", 8192, 7168, 256, 8, 64, RANK_CONTIGUOUS, SCORE_SIGMOID,
                         True, 8, 4, 0.0, 2048, 2048, "bf16", 0.0, 0.1, 1e-3)
 DSV3_DECODE = replace(DSV3_PREFILL, name="dsv3_decode", tokens=512, num_ranks=40,
                       rank_map=RANK_ROUND_ROBIN)
 DECODE_TOKENS = (1, 8, 64, 128, 512)
 
-WORKLOADS = {w.name: w for w in (TINY_TOP2_F32, SWITCH_TOP1, GSHARD_TOP2, DSV3_PREFILL,
-                                 DSV3_DECODE)}
+WORKLOADS = {w.name: w for w in (TINY_TOP2_F32, SWITCH_TOP1, GSHARD_TOP2, GSHARD_TOP2_PADDED,
+                                 DSV3_PREFILL, DSV3_DECODE)}
 
 
 def _normal_(t, std, gen, chunk_rows=64):

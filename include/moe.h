@@ -60,6 +60,7 @@ typedef enum {
 enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 };
 enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
 enum { MOE_RANK_CONTIGUOUS = 0, MOE_RANK_ROUND_ROBIN = 1 };
+enum { MOE_DISPATCH_PACKED = 0, MOE_DISPATCH_CAPACITY_PADDED = 1 };
 
 /* Layer configuration (host struct, passed by const pointer; read during the call
  * only).  Limits: 1 <= tokens; 8 <= hidden, hidden % 8 == 0;
@@ -86,7 +87,18 @@ typedef struct {
   int32_t shared_d_ff;     /* Fs: always-on shared expert size, 0 = none */
   int32_t act_dtype;       /* MOE_DTYPE_F32 or MOE_DTYPE_BF16 (activations and expert
                               weights); the router weight and logits are always fp32 */
+  int32_t dispatch_mode;   /* MOE_DISPATCH_PACKED: capacity goes to assignments in token
+                              order and the send buffer is packed (N*k rows).
+                              MOE_DISPATCH_CAPACITY_PADDED (needs capacity_factor > 0):
+                              every expert owns C consecutive rows (E*C rows, padding
+                              unused), and capacity goes to all first choices in token
+                              order, then all second choices, and so on */
 } moe_config;
+
+/* Rows of the send buffer (xperm, yperm) and length of perm_src for `cfg`: N*k for
+ * MOE_DISPATCH_PACKED, E*C for MOE_DISPATCH_CAPACITY_PADDED.  `rows` is a HOST
+ * pointer. */
+MOE_API moe_status moe_send_rows(const moe_config* cfg, int64_t* rows);
 
 /* Bytes of workspace that every call below needs for `cfg` (one size serves all
  * calls; a larger workspace is fine).  `bytes` is a HOST pointer.  The workspace is
@@ -126,22 +138,26 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const float* 
 /* Dispatch.  Same page, step 2 (each token's hidden state goes to the rank holding
  * its expert) and the page's counting example (assignments per expert and per
  * device); section "Load balancing and capacity" (capacity factor: an expert takes
- * at most cf times its even share, overflow skips that expert).  Deterministic:
- * assignments a = t*k + j are processed in token order.
+ * at most cf times its even share, overflow skips that expert); bowenzhou.top
+ * "专家并行", exercise 2 (each expert's buffer is reserved at the mean times 1.25:
+ * the capacity-padded layout).  Deterministic: assignments a = t*k + j compete in
+ * token order (packed) or choice-major order (padded).
  *
  *   topk_idx      [N, k]     int32      from moe_route
  *   x             [N, d]     act_dtype  hidden states
- *   xperm         [N*k, d]   act_dtype  out: send buffer, rows [0, num_kept) written,
- *                                       ordered by rank, then expert, then token
+ *   xperm         [S, d]     act_dtype  out: send buffer (S = moe_send_rows): packed,
+ *                                       rows [0, num_kept) written, ordered by rank, then
+ *                                       expert, then priority; padded, expert e's kept rows
+ *                                       at expert_start[e] + [0, kept_counts[e])
  *   expert_counts [E]        int32      out: routed assignments per expert (pre-cap)
  *   kept_counts   [E]        int32      out: min(count, C)
  *   expert_start  [E]        int32      out: first xperm row of each expert
  *   rank_counts   [R]        int32      out: kept rows per logical rank
  *   rank_offsets  [R + 1]    int32      out: exclusive prefix of rank_counts
  *   slot_of       [N*k]      int32      out: xperm row of assignment a, -1 if dropped
- *   perm_src      [N*k]      int32      out: assignment held by xperm row s
- *                                       (s < num_kept), -1 for s >= num_kept
- *   num_kept      [1]        int32      out: rows written to xperm
+ *   perm_src      [S]        int32      out: assignment held by xperm row s, -1 for a row
+ *                                       holding none
+ *   num_kept      [1]        int32      out: assignments kept (rows written to xperm)
  * xperm may be NULL to compute the routing tables only (x is then ignored). */
 MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x,
                         void* xperm, int32_t* expert_counts, int32_t* kept_counts,
@@ -175,13 +191,13 @@ MOE_API moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* to
  * every token).  Each expert is a SwiGLU feed-forward block:
  *   h = silu(X Wg^T) * (X Wu^T),  Y = h Wd^T
  *
- *   xperm          [N*k, d]       act_dtype  from moe_dispatch
+ *   xperm          [S, d]         act_dtype  from moe_dispatch (S = moe_send_rows)
  *   expert_start   [E], kept_counts [E]  int32  from moe_dispatch (read on device)
  *   w_gate_up      [E, 2F, d]     act_dtype  rows 0..F-1 gate Wg, F..2F-1 up Wu
  *   w_down         [E, d, F]      act_dtype  Wd
  *   x              [N, d]         act_dtype  input of the shared expert (NULL if none)
  *   shared_gate_up [2Fs, d], shared_down [d, Fs]  act_dtype, NULL if shared_d_ff == 0
- *   yperm          [N*k, d]       act_dtype  out: rows [0, num_kept) written
+ *   yperm          [S, d]         act_dtype  out: the kept rows written
  *   yshared        [N, d]         act_dtype  out: shared expert output (NULL if none)
  * bf16: tensor-core products with fp32 accumulation; h is rounded to bf16.
  * fp32: fp32 products and accumulation. */
@@ -212,7 +228,7 @@ MOE_API moe_status moe_selftest_ffn_stall(const moe_config* cfg, const void* xpe
  *   out[t] = residual[t] + yshared[t] + sum_{j kept} topk_w[t,j] * yperm[slot_of[t,j]]
  * summed in fp32 in the order written (j ascending), rounded once to act_dtype.  A
  * token with no kept choice and no shared expert gets out[t] == residual[t] exactly.
- *   yperm [N*k, d], slot_of [N*k], topk_w [N, k], residual [N, d] or NULL,
+ *   yperm [S, d], slot_of [N*k], topk_w [N, k], residual [N, d] or NULL,
  *   yshared [N, d] or NULL, out [N, d]. */
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* yperm, const int32_t* slot_of,
                        const float* topk_w, const void* residual, const void* yshared,

@@ -55,7 +55,7 @@ def _route(moe, cfg, ws_bytes=1 << 40, x=FAKE, ws=FAKE, wr=FAKE):
     ("tokens", 0), ("hidden", 12), ("hidden", 4), ("num_experts", 257), ("num_experts", 0),
     ("top_k", 0), ("top_k", 9), ("num_ranks", 0), ("num_ranks", 300), ("rank_map", 2),
     ("score_fn", 3), ("num_groups", 3), ("topk_groups", 9), ("d_ff", 12), ("shared_d_ff", 4),
-    ("act_dtype", 5), ("capacity_factor", float("inf"))])
+    ("act_dtype", 5), ("capacity_factor", float("inf")), ("dispatch_mode", 2)])
 def test_invalid_config_rejected_on_host(moe_lib, field, value):
     cfg = moe_lib.config(W.DSV3_PREFILL)
     setattr(cfg, field, value)
@@ -63,6 +63,14 @@ def test_invalid_config_rejected_on_host(moe_lib, field, value):
     n = ctypes.c_size_t(0)
     assert moe_lib.lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == \
         moe_lib.MOE_ERR_INVALID_ARG
+
+
+def test_padded_dispatch_needs_capacity_and_sizes_send_rows(moe_lib):
+    cfg = moe_lib.config(W.GSHARD_TOP2_PADDED)
+    assert moe_lib.moe_send_rows(cfg) == 64 * 1280          # E * C
+    assert moe_lib.moe_send_rows(moe_lib.config(W.GSHARD_TOP2)) == 32768 * 2
+    cfg.capacity_factor = 0.0                               # no capacity, no padded layout
+    assert _route(moe_lib, cfg) == moe_lib.MOE_ERR_INVALID_ARG
 
 
 def test_group_limit_must_leave_k_candidates(moe_lib):

@@ -93,25 +93,28 @@ def check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=
     assert mism.size == 0, f"top-k ids differ at {mism[:5].tolist()}"
     close(host(b.topk_w), w_ref, TOL_W, "combine weights")
     # ---- dispatch tables from the GPU's own ids: bit-exact
-    d = oracle.dispatch(idx_gpu, E, w.num_ranks, w.rank_map, w.capacity_factor)
+    d = oracle.dispatch(idx_gpu, E, w.num_ranks, w.rank_map, w.capacity_factor,
+                        mode=w.dispatch_mode)
     for name in ("expert_counts", "kept_counts", "expert_start", "rank_counts", "rank_offsets",
                  "slot_of", "perm_src"):
         np.testing.assert_array_equal(host(getattr(b, name)), d[name], err_msg=name)
     nk = int(host(b.num_kept)[0])
     assert nk == d["num_kept"]
     assert host(b.expert_counts).sum() == N * k
-    # ---- send buffer rows are exact copies
-    ps = d["perm_src"][:nk]
-    xp = host(b.xperm[:nk])
+    # ---- send buffer rows are exact copies (the rows that hold an assignment)
+    kept_rows = np.nonzero(d["perm_src"] >= 0)[0]
+    assert kept_rows.size == nk
+    ps = d["perm_src"][kept_rows]
+    xp = host(b.xperm[torch.from_numpy(kept_rows).cuda().long()]) if nk else x_h[:0]
     np.testing.assert_array_equal(xp, x_h[ps // k], err_msg="xperm")
     # ---- expert FFN on the GPU's send rows
     flat_idx = idx_gpu.reshape(-1)
-    srows = np.arange(nk) if n_sample_rows is None else np.sort(
+    sel = np.arange(nk) if n_sample_rows is None else np.sort(
         rng.choice(nk, size=min(nk, n_sample_rows), replace=False))
     wgu, wd, sgu, sd = hw["w_gate_up"], hw["w_down"], hw["shared_gate_up"], hw["shared_down"]
-    if srows.size:
-        y_ref = oracle.expert_rows(xp[srows], flat_idx[ps[srows]], wgu, wd)
-        y_got = f64(b.yperm[torch.from_numpy(srows).cuda().long()])
+    if sel.size:
+        y_ref = oracle.expert_rows(xp[sel], flat_idx[ps[sel]], wgu, wd)
+        y_got = f64(b.yperm[torch.from_numpy(kept_rows[sel]).cuda().long()])
         close(y_got, y_ref, TOL_OUT[w.act_dtype], "expert FFN rows")
     if sgu is not None:
         trows = np.arange(N) if n_sample_rows is None else np.sort(
@@ -161,7 +164,8 @@ def test_tiny_top2_f32_full():
     assert (ec.min(), ec.max(), rc.min(), rc.max()) == (948, 1087, 1968, 2139)
 
 
-@pytest.mark.parametrize("w", [W.SWITCH_TOP1, W.GSHARD_TOP2], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.SWITCH_TOP1, W.GSHARD_TOP2, W.GSHARD_TOP2_PADDED],
+                         ids=lambda w: w.name)
 def test_capacity_workloads(w):
     inp = W.make_inputs(w, seed=0, device="cuda")
     b, _ = run_gpu(w, inp)
@@ -255,6 +259,18 @@ EDGE = {
     "small_segments_ragged": small(tokens=40, hidden=264, num_experts=64, top_k=4, num_ranks=8,
                                    num_groups=8, topk_groups=4, capacity_factor=1.0, d_ff=200,
                                    shared_d_ff=72),
+    "softmax_group_limited": small(tokens=700, hidden=136, num_experts=32, top_k=3, num_ranks=8,
+                                   score_fn=0, normalize_topk=False, num_groups=8,
+                                   topk_groups=2, d_ff=64, shared_d_ff=0, sel_bias_std=0.0),
+    "padded_choice_major_round_robin": small(tokens=900, hidden=128, num_experts=24, top_k=3,
+                                             num_ranks=7, rank_map=1, score_fn=0,
+                                             num_groups=1, topk_groups=1, capacity_factor=0.9,
+                                             d_ff=96, shared_d_ff=64, sel_bias_std=0.0,
+                                             dispatch_mode=1),
+    "padded_f32_small_segments": small(tokens=12, hidden=72, num_experts=16, top_k=2,
+                                       num_ranks=4, score_fn=0, num_groups=1, topk_groups=1,
+                                       capacity_factor=1.0, d_ff=40, shared_d_ff=0,
+                                       act_dtype="f32", sel_bias_std=0.0, dispatch_mode=1),
     "capacity_exact_boundary": small(tokens=256, hidden=64, num_experts=4, top_k=1, num_ranks=4,
                                      score_fn=0, num_groups=1, topk_groups=1,
                                      capacity_factor=1.0, d_ff=32, shared_d_ff=0,
