@@ -48,15 +48,26 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
+                    help="override a workload field (e.g. num_experts=16), for small "
+                         "profiling cases of the same kernels")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the C-ABI calls every step instead of replaying a CUDA graph")
     return ap.parse_args()
 
 
-def workload(name):
+def workload(name, overrides=()):
+    import dataclasses
     base, _, n = name.partition("@")
     w = W.WORKLOADS[base]
-    return w.with_tokens(int(n)) if n else w
+    w = w.with_tokens(int(n)) if n else w
+    for kv in overrides:
+        k, _, v = kv.partition("=")
+        t = type(getattr(w, k))
+        w = dataclasses.replace(w, **{k: t(float(v)) if t is int else t(v)})
+    if overrides:
+        w = dataclasses.replace(w, name=w.name + "+" + ",".join(overrides))
+    return w
 
 
 def measured_ffn_traffic():
@@ -462,7 +473,7 @@ def run_reference(a, w):
 
 def main():
     a = parse()
-    w = workload(a.config)
+    w = workload(a.config, a.set)
     if a.impl == "reference":
         # rank 0 alone times the CPU oracle; other ranks exit without work
         if int(os.environ.get("RANK", "0")) == 0:
