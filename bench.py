@@ -186,7 +186,8 @@ def oracle_step(oracle, w, h, n):
     logits = oracle.router_logits(x, h["w_router"], h["b_router"])
     idx, wts = oracle.route(logits, w.top_k, w.score_fn, w.normalize_topk, w.num_groups,
                             w.topk_groups, h["sel_bias"])
-    d = oracle.dispatch(idx, w.num_experts, w.num_ranks, w.rank_map, w.capacity_factor)
+    d = oracle.dispatch(idx, w.num_experts, w.num_ranks, w.rank_map, w.capacity_factor,
+                        w.dispatch_mode)
     oracle.layer_tokens(np.arange(n, dtype=np.int32), x, idx, wts, d["slot_of"],
                         h["w_gate_up"], h["w_down"], h["shared_gate_up"], h["shared_down"])
     if w.bias_step and h["sel_bias"] is not None:
@@ -246,25 +247,25 @@ def run_native(a, w, rank, world, local):
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     s = torch.cuda.current_stream()
 
-    def step(evs=None):
-        c = b.cfg
-        if evs: evs[0].record(s)
-        moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"], b.logits,
-                      b.topk_idx, b.topk_w, b.workspace)
-        if evs: evs[1].record(s)
-        moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
-                         b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
-                         b.num_kept, b.workspace)
-        if evs: evs[2].record(s)
-        moe.moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
-                           inp["w_down"], inp["x"], inp["shared_gate_up"], inp["shared_down"],
-                           b.yperm, b.yshared, b.workspace)
-        if evs: evs[3].record(s)
-        moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out)
-        if evs: evs[4].record(s)
-        if step_bias and inp["sel_bias"] is not None:
-            moe.moe_bias_update(c, b.expert_counts, inp["sel_bias"], step_bias)
-        if evs: evs[5].record(s)
+    c = b.cfg
+    stages = [
+        lambda: moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"],
+                              b.logits, b.topk_idx, b.topk_w, b.workspace),
+        lambda: moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts,
+                                 b.kept_counts, b.expert_start, b.rank_counts, b.rank_offsets,
+                                 b.slot_of, b.perm_src, b.num_kept, b.workspace),
+        lambda: moe.moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
+                                   inp["w_down"], inp["x"], inp["shared_gate_up"],
+                                   inp["shared_down"], b.yperm, b.yshared, b.workspace),
+        lambda: moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out),
+    ]
+    if step_bias and inp["sel_bias"] is not None:
+        stages.append(lambda: moe.moe_bias_update(c, b.expert_counts, inp["sel_bias"], step_bias))
+    n_st = len(stages)
+
+    def step():
+        for f in stages:
+            f()
 
     for _ in range(a.warmup):
         step()
@@ -274,48 +275,46 @@ def run_native(a, w, rank, world, local):
     assert int(b.workspace[:4].view(torch.int32).item()) == 0, "device status word set"
     num_kept = int(b.num_kept.item())
 
-    # one step captured as a CUDA graph (the five C-ABI calls, launched once each)
-    graph = None
+    # each C-ABI call captured as its own CUDA graph, so that events between the graph
+    # launches time every stage inside the timed region
+    runs = stages
     if not a.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
+        runs = []
+        for f in stages:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                f()
+            runs.append(g.replay)
         torch.cuda.synchronize()
         for _ in range(a.warmup):
-            graph.replay()
+            for r in runs:
+                r()
         torch.cuda.synchronize()
         if bias0 is not None:
             inp["sel_bias"].copy_(bias0)
-    run = graph.replay if graph is not None else step
 
-    # ---------------- timed: K steps, CUDA events around each step on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(a.steps)]
+    # ---------------- timed: K steps; CUDA events between the C-ABI calls of every step,
+    # on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)]
+           for _ in range(a.steps)]
     clk = Clocks(dev.index) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
     for i in range(a.steps):
         flush.fill_(i & 0xff)            # L2 flush, outside the step's events
         evs[i][0].record(s)
-        run()
-        evs[i][1].record(s)
+        for j, r in enumerate(runs):
+            r()
+            evs[i][j + 1].record(s)
     torch.cuda.synchronize()
     barrier(world)
-    step_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(n_st)] for e in evs])  # ms
+    step_ms = per.sum(axis=1)
     total_s = max_over_ranks(step_ms.sum() / 1e3, world)
     value = weak_scaling_value(w.tokens, a.steps, world, total_s)
+    route_ms, disp_ms, ffn_ms, comb_ms = per.mean(axis=0)[:4]
+    bias_ms = float(per.mean(axis=0)[4]) if n_st > 4 else 0.0
     status = int(b.workspace[:4].view(torch.int32).item())
-    if bias0 is not None:
-        inp["sel_bias"].copy_(bias0)
-
-    # ---------------- per-stage times: direct C-ABI calls with events between calls
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(a.steps)]
-    torch.cuda.synchronize()
-    for i in range(a.steps):
-        flush.fill_(i & 0xff)
-        step(sevs[i])
-    torch.cuda.synchronize()
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in sevs])  # ms
-    route_ms, disp_ms, ffn_ms, comb_ms, bias_ms = per.mean(axis=0)
     if bias0 is not None:
         inp["sel_bias"].copy_(bias0)
 
@@ -385,7 +384,7 @@ def run_native(a, w, rank, world, local):
     torch.cuda.synchronize()
     torch.cuda.set_stream(torch.cuda.default_stream(dev))
     barrier(world)
-    clocks = clk.stop() if clk else None  # sampled over the timed, per-stage and e2e loops
+    clocks = clk.stop() if clk else None  # sampled over the timed and e2e loops
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e_value = weak_scaling_value(w.tokens, a.steps, world, e2e_s)
     if bias0 is not None:
@@ -411,7 +410,7 @@ def run_native(a, w, rank, world, local):
                    "l2": "flushed between steps (252 MiB write outside the step events); "
                          "per-step working set larger than L2",
                    "parallelism": f"replica x{world} (token-sharded, no collective)",
-                   "launch": "CUDA graph of the five C-ABI calls" if graph is not None
+                   "launch": "one CUDA graph per C-ABI call" if not a.no_graph
                              else "direct C-ABI calls"},
         "roofline": {"kernel": "expert grouped GEMMs (gate_up+SwiGLU, down) of moe_expert_ffn",
                      "bound": "tensor", "achieved": ffn_tflops, "peak": pk["bf16"],
@@ -427,7 +426,7 @@ def run_native(a, w, rank, world, local):
                              "frac_of_8TBs": dc_gbs / 8000.0},
         "stage_ms": {"route": route_ms, "dispatch": disp_ms, "expert_ffn": ffn_ms,
                      "combine": comb_ms, "bias_update": bias_ms,
-                     "note": "direct calls with events between them (not graph replay)"},
+                     "note": "events between the calls of each timed step"},
         "routing": {"num_kept": num_kept, "drop_rate": 1.0 - num_kept / (w.tokens * w.top_k)},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                 "d2h_bytes_per_step": io_bytes,

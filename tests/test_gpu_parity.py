@@ -271,6 +271,12 @@ EDGE = {
                                        num_ranks=4, score_fn=0, num_groups=1, topk_groups=1,
                                        capacity_factor=1.0, d_ff=40, shared_d_ff=0,
                                        act_dtype="f32", sel_bias_std=0.0, dispatch_mode=1),
+    # smallest legal sizes: hidden = d_ff = 8 (one 16-byte vector per row)
+    "minimal_sizes_bf16": small(tokens=5, hidden=8, num_experts=4, top_k=2, num_ranks=2,
+                                num_groups=2, topk_groups=1, d_ff=8, shared_d_ff=8),
+    "minimal_sizes_f32": small(tokens=5, hidden=8, num_experts=4, top_k=2, num_ranks=2,
+                               score_fn=0, num_groups=1, topk_groups=1, d_ff=8, shared_d_ff=8,
+                               act_dtype="f32", sel_bias_std=0.0),
     "capacity_exact_boundary": small(tokens=256, hidden=64, num_experts=4, top_k=1, num_ranks=4,
                                      score_fn=0, num_groups=1, topk_groups=1,
                                      capacity_factor=1.0, d_ff=32, shared_d_ff=0,
