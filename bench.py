@@ -216,6 +216,53 @@ def cpu_baseline(w, h, budget_s=15.0):
 
 
 # ------------------------------------------------------------------ native arm
+def counts_allreduce(world):
+    """Sum of the replicas' expert_counts, in place and asynchronous (the caller waits
+    on the returned handle before the bias update); None on a single replica."""
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    return lambda t: dist.all_reduce(t, op=dist.ReduceOp.SUM, async_op=True)
+
+
+def capture_layer(moe, b, inp, bias_step, reduce, world):
+    """The layer step as CUDA graph replays.  One replica: one graph of the whole
+    step.  Several: route+dispatch, expert FFN+combine and the bias update as three
+    graphs, with the counts all-reduce issued eagerly between them."""
+    if reduce is None:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            moe.run_layer(b, inp, bias_step=bias_step)
+        return g.replay
+    c, cb = b.cfg, moe.with_tokens(b.cfg, b.cfg.tokens * world)
+    parts = [
+        lambda: (moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"],
+                               b.logits, b.topk_idx, b.topk_w, b.workspace),
+                 moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts,
+                                  b.kept_counts, b.expert_start, b.rank_counts, b.rank_offsets,
+                                  b.slot_of, b.perm_src, b.num_kept, b.workspace)),
+        lambda: (moe.moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
+                                    inp["w_down"], inp["x"], inp["shared_gate_up"],
+                                    inp["shared_down"], b.yperm, b.yshared, b.workspace),
+                 moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out)),
+        lambda: moe.moe_bias_update(cb, b.expert_counts, inp["sel_bias"], bias_step),
+    ]
+    graphs = []
+    for f in parts:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            f()
+        graphs.append(g)
+
+    def run():
+        graphs[0].replay()
+        h = reduce(b.expert_counts)
+        graphs[1].replay()
+        h.wait()
+        graphs[2].replay()
+    return run
+
+
 def launches_per_step(w):
     n = 1                      # route
     n += 4                     # dispatch: count, scan, assign, permute
@@ -240,7 +287,11 @@ def run_native(a, w, rank, world, local):
     from expert_routing_router_b300 import moe
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
-    inp = W.make_inputs(w, seed=a.seed + rank, device=dev)
+    # every replica holds the same layer (weights, router, selection bias) and its own
+    # token batch
+    inp = W.make_inputs(w, seed=a.seed, device=dev)
+    if rank > 0:
+        inp["x"] = W.make_tokens(w, w.tokens, seed=a.seed + rank, device=dev)
     b = moe.LayerBuffers(w, device=dev)
     step_bias = w.bias_step
     bias0 = None if inp["sel_bias"] is None else inp["sel_bias"].clone()
@@ -259,16 +310,30 @@ def run_native(a, w, rank, world, local):
                                    inp["shared_down"], b.yperm, b.yshared, b.workspace),
         lambda: moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out),
     ]
-    if step_bias and inp["sel_bias"] is not None:
-        stages.append(lambda: moe.moe_bias_update(c, b.expert_counts, inp["sel_bias"], step_bias))
+    has_bias = bool(step_bias) and inp["sel_bias"] is not None
+    # the bias update applies the sign rule to the routed counts of all replicas
+    reduce = counts_allreduce(world) if has_bias else None
+    cb = moe.with_tokens(c, w.tokens * world) if world > 1 else c
+    if has_bias:
+        stages.append(lambda: moe.moe_bias_update(cb, b.expert_counts, inp["sel_bias"],
+                                                  step_bias))
     n_st = len(stages)
 
-    def step():
-        for f in stages:
-            f()
+    def step(runs, evs=None):
+        h = None
+        if evs is not None:
+            evs[0].record(s)
+        for j, r in enumerate(runs):
+            if j == 4 and h is not None:
+                h.wait()              # the summed counts feed the bias update
+            r()
+            if j == 1 and reduce is not None:
+                h = reduce(b.expert_counts)   # overlaps the expert FFN and combine
+            if evs is not None:
+                evs[j + 1].record(s)
 
     for _ in range(a.warmup):
-        step()
+        step(stages)
     torch.cuda.synchronize()
     if bias0 is not None:
         inp["sel_bias"].copy_(bias0)
@@ -287,8 +352,7 @@ def run_native(a, w, rank, world, local):
             runs.append(g.replay)
         torch.cuda.synchronize()
         for _ in range(a.warmup):
-            for r in runs:
-                r()
+            step(runs)
         torch.cuda.synchronize()
         if bias0 is not None:
             inp["sel_bias"].copy_(bias0)
@@ -302,10 +366,7 @@ def run_native(a, w, rank, world, local):
     torch.cuda.synchronize()
     for i in range(a.steps):
         flush.fill_(i & 0xff)            # L2 flush, outside the step's events
-        evs[i][0].record(s)
-        for j, r in enumerate(runs):
-            r()
-            evs[i][j + 1].record(s)
+        step(runs, evs[i])
     torch.cuda.synchronize()
     barrier(world)
     per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(n_st)] for e in evs])  # ms
@@ -336,15 +397,13 @@ def run_native(a, w, rank, world, local):
         inp_i = dict(inp, x=xi)
 
         def step_i(bb=bi, ii=inp_i):
-            moe.run_layer(bb, ii, bias_step=step_bias)
-        gi = None
+            moe.run_layer(bb, ii, bias_step=step_bias, reduce_counts=reduce, replicas=world)
+        run_i = step_i
         if not a.no_graph:
             step_i()
             torch.cuda.synchronize()
-            gi = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gi):
-                step_i()
-        sets.append((xi, bi, gi.replay if gi is not None else step_i))
+            run_i = capture_layer(moe, bi, inp_i, step_bias, reduce, world)
+        sets.append((xi, bi, run_i))
     if bias0 is not None:
         inp["sel_bias"].copy_(bias0)
     # compute and copies on two streams of their own (the legacy default stream would

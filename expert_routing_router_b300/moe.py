@@ -197,19 +197,49 @@ class LayerBuffers:
         self.workspace[:256].zero_()          # sticky device status word starts at 0
 
 
-def run_layer(b, inp, bias_step=0.0, stream=None):
+def with_tokens(cfg, tokens):
+    """Copy of a moe_config with another token count: the union of the data-parallel
+    replicas' batches, for the bias update over all-reduced counts."""
+    c = moe_config.from_buffer_copy(cfg)
+    c.tokens = int(tokens)
+    return c
+
+
+def run_layer(b, inp, bias_step=0.0, stream=None, reduce_counts=None, replicas=1):
     """One pass of the layer path through the C ABI: route, dispatch, expert FFN,
-    combine, and (if bias_step) the selection-bias update."""
+    combine, and (if bias_step) the selection-bias update.
+
+    Data-parallel replicas (each its own token batch, the same layer): the bias update
+    needs the load of every replica's batch.  `reduce_counts(expert_counts)` sums the
+    routed counts over the replicas in place (an all-reduce; it may return a handle
+    whose .wait() orders it before the bias update, so that it overlaps the expert
+    FFN), and the sign rule then compares the summed counts with the mean load of all
+    `replicas` batches.  b.expert_counts holds the summed counts afterwards."""
     c = b.cfg
     moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"], b.logits,
               b.topk_idx, b.topk_w, b.workspace, stream)
     moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
                  b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
                  b.num_kept, b.workspace, stream)
+    update = bool(bias_step) and inp["sel_bias"] is not None
+    handle = None
+    if update and reduce_counts is not None:
+        if stream is None:
+            handle = reduce_counts(b.expert_counts)
+        else:
+            with torch.cuda.stream(stream):
+                handle = reduce_counts(b.expert_counts)
     moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"], inp["w_down"],
                    inp["x"], inp["shared_gate_up"], inp["shared_down"], b.yperm, b.yshared,
                    b.workspace, stream)
     moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out, stream)
-    if bias_step and inp["sel_bias"] is not None:
-        moe_bias_update(c, b.expert_counts, inp["sel_bias"], bias_step, stream)
+    if update:
+        if handle is not None:
+            if stream is None:
+                handle.wait()
+            else:
+                with torch.cuda.stream(stream):
+                    handle.wait()
+        cb = with_tokens(c, c.tokens * replicas) if replicas > 1 else c
+        moe_bias_update(cb, b.expert_counts, inp["sel_bias"], bias_step, stream)
     return b.out

@@ -1,13 +1,16 @@
 """Host-side logic of the multi-rank benchmark, on CPU with gloo (world size 2).
 
-Each rank is an independent replica on its own token slice (no collective on the
-data path); the only cross-rank steps are the barrier and the max over ranks of the
-timed region, from which rank 0 reports whole-job tokens/s.
+Each rank is an independent replica of the layer on its own token slice.  The
+forward path has no collective; the bias update sums the replicas' routed counts
+(one all-reduce of E int32) and applies the sign rule against the mean load of all
+replicas' tokens.  The barrier and the max over ranks of the timed region give
+rank 0's whole-job tokens/s.
 """
 import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch
 import torch.distributed as dist
@@ -46,6 +49,69 @@ def test_max_over_ranks_and_weak_scaling_gloo():
         assert p.exitcode == 0
     assert [r[1] for r in res] == [2.0, 2.0]            # both ranks see the max
     assert res[0][2] == pytest.approx(8192 * 10 * 2 / 2.0)
+
+
+def _slice_logits(rank, N, E):
+    """Rank r's router logits: noise plus a strong preference for expert r, so that
+    each replica alone would see a different expert overloaded."""
+    rng = np.random.default_rng(100 + rank)
+    lg = rng.standard_normal((N, E)).astype(np.float32)
+    lg[:, rank] += 3.0
+    return lg
+
+
+def _bias_worker(rank, world, port, q, N, E, k, step):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import oracle
+        idx, _ = oracle.route(_slice_logits(rank, N, E), k)
+        local = oracle.dispatch(idx, E, 1)["expert_counts"]
+        t = torch.from_numpy(local.copy())
+        bench.counts_allreduce(world)(t).wait()
+        bias0 = np.linspace(-0.05, 0.05, E, dtype=np.float32)
+        glob = oracle.bias_update(t.numpy(), bias0, N * world, k, step)
+        alone = oracle.bias_update(local, bias0, N, k, step)
+        q.put((rank, t.numpy().tolist(), glob.tolist(), alone.tolist()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_bias_update_over_allreduced_counts_gloo():
+    """Replicas end with one bias, equal to the update of the concatenated batch;
+    updating from local counts alone would have split them."""
+    import oracle
+    N, E, k, step = 96, 8, 2, 1e-3
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 31500 + (os.getpid() % 2000)
+    procs = [ctx.Process(target=_bias_worker, args=(r, 2, port, q, N, E, k, step))
+             for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=180) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    lg = np.concatenate([_slice_logits(r, N, E) for r in range(2)])
+    idx, _ = oracle.route(lg, k)
+    counts = oracle.dispatch(idx, E, 1)["expert_counts"]
+    bias0 = np.linspace(-0.05, 0.05, E, dtype=np.float32)
+    want = oracle.bias_update(counts, bias0, 2 * N, k, step)
+    for _, c, glob, _alone in res:
+        assert c == counts.tolist()
+        assert np.array_equal(np.array(glob, np.float32), want)
+    assert res[0][3] != res[1][3]          # local-only updates disagree across replicas
+
+
+def test_with_tokens_copies_config(moe_lib):
+    from expert_routing_router_b300 import workloads as W
+    c = moe_lib.config(W.DSV3_PREFILL)
+    g = moe_lib.with_tokens(c, 4 * c.tokens)
+    assert g.tokens == 4 * 8192 and c.tokens == 8192
+    assert [getattr(g, f) for f, _ in g._fields_ if f != "tokens"] == \
+        [getattr(c, f) for f, _ in c._fields_ if f != "tokens"]
 
 
 def test_weak_scaling_value_single():
