@@ -43,6 +43,10 @@ def _lib():
         lib.oracle_combine.argtypes = [I, P, I, I, I, P, P, P, P, P, P]
         lib.oracle_layer_tokens.argtypes = [I, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P]
         lib.oracle_bias_update.argtypes = [I, I, I, P, F, P]
+        lib.oracle_quant_rows.argtypes = [I, I, I, P, P, P, P]
+        lib.oracle_dequant_rows.argtypes = [I, I, I, P, P, P, P]
+        lib.oracle_combine_q8.argtypes = [I, P, I, I, I, P, P, P, P, P, P, P]
+        lib.oracle_float_to_bf16.argtypes = [ctypes.c_int64, P, P]
         _LIB = lib
     return _LIB
 
@@ -203,3 +207,52 @@ def bias_update(counts, bias, N, k, step):
     b = np.array(bias, dtype=np.float32, copy=True)
     _lib().oracle_bias_update(b.size, N, k, _p(counts), float(step), _p(b))
     return b
+
+
+def quant_rows(rows, valid=None):
+    """Per-row symmetric INT8 codes and fp32 scales of rows [R, d] (fp32 or bf16 bits).
+    Rows with valid[r] < 0 are skipped (codes 0, scale NaN in the returned arrays)."""
+    rows, code = _act(rows)
+    R, d = rows.shape
+    q = np.zeros((R, d), np.int8)
+    s = np.full(R, np.nan, np.float32)
+    v = None if valid is None else np.ascontiguousarray(valid, dtype=np.int32)
+    _lib().oracle_quant_rows(R, d, code, _p(rows), _p(v), _p(q), _p(s))
+    return q, s
+
+
+def dequant_rows(q, scale, act_dtype="bf16", valid=None):
+    """(float)q * scale per row, stored as fp32 or bf16 bits (uint16)."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    R, d = q.shape
+    code = ACT_F32 if act_dtype == "f32" else ACT_BF16
+    out = np.zeros((R, d), np.float32 if code == ACT_F32 else np.uint16)
+    v = None if valid is None else np.ascontiguousarray(valid, dtype=np.int32)
+    _lib().oracle_dequant_rows(R, d, code, _p(q), _p(scale), _p(v), _p(out))
+    return out
+
+
+def combine_q8(tokens, x, yq, yscale, slot_of, w, ys=None):
+    x, code = _act(x)
+    N, d = x.shape
+    yq = np.ascontiguousarray(yq, dtype=np.int8)
+    yscale = np.ascontiguousarray(yscale, dtype=np.float32)
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32).reshape(-1)
+    w = np.ascontiguousarray(w, dtype=np.float64).reshape(-1)
+    k = slot_of.size // N
+    if ys is not None:
+        ys, c3 = _act(ys)
+        assert c3 == code
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    out = np.empty((tokens.size, d), dtype=np.float64)
+    _lib().oracle_combine_q8(tokens.size, _p(tokens), d, k, code, _p(x), _p(yq), _p(yscale),
+                             _p(ys), _p(slot_of), _p(w), _p(out))
+    return out
+
+
+def float_to_bf16(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _lib().oracle_float_to_bf16(a.size, _p(a), _p(out))
+    return out

@@ -14,6 +14,8 @@
 //   6. expert FFN         SwiGLU, fp64, no intermediate rounding
 //   7. combine            out[t] = x[t] + shared(x[t]) + sum_j w[t,j] y_j, fp64
 //   8. bias update        sign rule, fp32
+//   9. INT8 payload       per-row symmetric quantisation of the rows an all-to-all
+//                         sends, and the receiver's dequantisation and combine
 //
 // Sources ("the pages"):
 //   [UG] Ultralytics glossary "Expert Parallelism" (Chinese, German and Japanese
@@ -23,6 +25,9 @@
 //   [BZ] bowenzhou.top knowledge planet, "专家并行" (expert parallelism); sections
 //        "机制：all-to-all 两轮" and the worked answer to exercise 2 (capacity factor).
 //   [FD] fudan-mlsys-cn chapter 10, section 10.5 (expert parallelism, shared experts).
+//   [BZ-D] the same bowenzhou.top note, section "深入推导：all-to-all 通信模型与
+//        DeepSeek-V3 的 EP 配置", paragraph on DeepSeek-V3's two-level EP (INT8
+//        quantised communication halves the traffic again).
 //
 // Readings where the pages are silent (each one is a choice, listed in the design notes):
 //   * ties in every ordering break toward the lower expert (or group) index;
@@ -70,6 +75,36 @@ inline double bf16_bits_to_double(uint16_t v) {
 inline double load_act(const void* base, int act_dtype, int64_t i) {
   if (act_dtype == 0) return static_cast<double>(static_cast<const float*>(base)[i]);
   return bf16_bits_to_double(static_cast<const uint16_t*>(base)[i]);
+}
+
+// fp32 -> bf16, round to nearest, ties to even, from the definition: of the two bf16
+// values that bracket f (f with its low 16 bits cleared, and the next bf16 away from
+// zero), take the nearer; on a tie take the one whose last kept bit is 0.  Finite
+// inputs only; a value that rounds past the largest bf16 becomes infinity.
+inline uint16_t float_to_bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  const uint32_t lo_bits = u & 0xffff0000u;
+  const uint32_t hi_bits = lo_bits + 0x10000u;  // next magnitude up, same sign
+  float lo, hi;
+  std::memcpy(&lo, &lo_bits, 4);
+  std::memcpy(&hi, &hi_bits, 4);
+  // past the largest finite bf16 the next value up is infinity, which the rounding
+  // rule places at 2^128 (an unbounded exponent's next power of two)
+  const double hi_d = ((hi_bits & 0x7f800000u) == 0x7f800000u)
+                          ? std::copysign(std::ldexp(1.0, 128), static_cast<double>(f))
+                          : static_cast<double>(hi);
+  const double dl = std::fabs(static_cast<double>(f) - lo);
+  const double dh = std::fabs(hi_d - f);
+  uint32_t pick;
+  if (dl < dh) {
+    pick = lo_bits;
+  } else if (dh < dl) {
+    pick = hi_bits;
+  } else {
+    pick = ((lo_bits >> 16) & 1u) ? hi_bits : lo_bits;
+  }
+  return static_cast<uint16_t>(pick >> 16);
 }
 
 // ---------------------------------------------------------------- fp32 sigmoid spec
@@ -506,6 +541,95 @@ int oracle_bias_update(int E, int N, int k, const int32_t* counts, float step, f
       bias[e] = bias[e] + step;
     }
   }
+  return 0;
+}
+
+// ---------------------------------------------------------------- 9. INT8 payload
+//
+// [BZ-D]: quantising the all-to-all payload to INT8 halves its traffic again.  The
+// pages fix no format; the reading taken (symmetric, one fp32 scale per row):
+//   s   = max_i |v_i| / 127                  fp32 divide
+//   q_i = rint(v_i / s), clamped to +-127     fp32 divide, round half to even
+//   a row of zeros has s = 0 and q = 0
+// The receiver's value is (float)q_i * s, one fp32 multiply, rounded once to the
+// activation type.  A code is an integer decided in floating point, so it is decided
+// in fp32 (v is widened exactly from bf16).  Rows with valid[r] < 0 are skipped
+// (left untouched); valid may be null (every row).
+int oracle_quant_rows(int rows, int d, int act_dtype, const void* in, const int32_t* valid,
+                      int8_t* q, float* scale) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    if (valid && valid[r] < 0) continue;
+    const int64_t base = static_cast<int64_t>(r) * d;
+    float amax = 0.0f;
+    for (int i = 0; i < d; ++i) {
+      const float v = static_cast<float>(load_act(in, act_dtype, base + i));
+      amax = std::max(amax, std::fabs(v));
+    }
+    const float s = amax / 127.0f;
+    scale[r] = s;
+    for (int i = 0; i < d; ++i) {
+      int c = 0;
+      if (s > 0.0f) {
+        const float v = static_cast<float>(load_act(in, act_dtype, base + i));
+        const float ratio = v / s;
+        c = static_cast<int>(std::nearbyint(ratio));  // default mode: nearest, ties even
+        c = std::min(127, std::max(-127, c));
+      }
+      q[base + i] = static_cast<int8_t>(c);
+    }
+  }
+  return 0;
+}
+
+// out[r, i] = (float)q[r, i] * scale[r] in fp32, stored in act_dtype (bf16: one
+// round-to-nearest-even).  Rows with valid[r] < 0 are left untouched.
+int oracle_dequant_rows(int rows, int d, int act_dtype, const int8_t* q, const float* scale,
+                        const int32_t* valid, void* out) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < rows; ++r) {
+    if (valid && valid[r] < 0) continue;
+    const int64_t base = static_cast<int64_t>(r) * d;
+    for (int i = 0; i < d; ++i) {
+      const float v = static_cast<float>(q[base + i]) * scale[r];
+      if (act_dtype == 0) {
+        static_cast<float*>(out)[base + i] = v;
+      } else {
+        static_cast<uint16_t*>(out)[base + i] = float_to_bf16_rne(v);
+      }
+    }
+  }
+  return 0;
+}
+
+// Combine from an INT8 return payload: as oracle_combine, with each expert output
+// element taken as (float)yq * yscale (fp32 multiply), then summed in fp64:
+// out[t] = x[t] + ys[t] + sum_{j kept} w[t,j] * ((float)yq[s,c] * yscale[s]), s = slot_of[t,j].
+int oracle_combine_q8(int ntok, const int32_t* tokens, int d, int k, int act_dtype,
+                      const void* x, const int8_t* yq, const float* yscale, const void* ys,
+                      const int32_t* slot_of, const double* w, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < ntok; ++i) {
+    const int64_t t = tokens[i];
+    double* o = out + static_cast<int64_t>(i) * d;
+    for (int c = 0; c < d; ++c) {
+      double acc = load_act(x, act_dtype, t * d + c);
+      if (ys) acc += load_act(ys, act_dtype, t * d + c);
+      for (int j = 0; j < k; ++j) {
+        const int32_t s = slot_of[t * k + j];
+        if (s < 0) continue;
+        const float v = static_cast<float>(yq[static_cast<int64_t>(s) * d + c]) * yscale[s];
+        acc += w[t * k + j] * static_cast<double>(v);
+      }
+      o[c] = acc;
+    }
+  }
+  return 0;
+}
+
+// fp32 -> bf16 bits (round to nearest even), exposed for its own pin.
+int oracle_float_to_bf16(int64_t n, const float* in, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = float_to_bf16_rne(in[i]);
   return 0;
 }
 

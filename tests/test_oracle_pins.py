@@ -452,3 +452,97 @@ def test_choice_major_padded_dispatch_bruteforce(N, E, k, R, rank_map, cf):
         assert d["rank_counts"][r] == d["kept_counts"][ranks == r].sum()
         assert d["rank_offsets"][r] == min(first[e] for e in range(E) if ranks[e] == r) * C
     assert d["rank_offsets"][R] == E * C
+
+
+# ------------------------------------------------------------------ INT8 payload
+
+def _bf16_bits(a):
+    return torch.tensor(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+
+
+def test_q8_codes_closed_form():
+    """Rows whose scale is exact (max 127 -> s = 1, max 254 -> s = 2): every code is
+    v / s rounded half to even, clamped; a zero row has scale 0 and zero codes."""
+    rows = np.array([[127, -63.5, 31.75, 0, 0.5, -127, 1.5, 2.5, -0.5, 3.49],
+                     [254, 3, 5, -7, 1, -1, 0, 9, 11, -254],
+                     [0] * 10], np.float32)
+    want_q = np.array([[127, -64, 32, 0, 0, -127, 2, 2, 0, 3],
+                       [127, 2, 2, -4, 0, 0, 0, 4, 6, -127],
+                       [0] * 10], np.int8)
+    want_s = np.array([1.0, 2.0, 0.0], np.float32)
+    for arr in (rows, _bf16_bits(rows[:, :8])):
+        q, s = oracle.quant_rows(arr)
+        np.testing.assert_array_equal(q, want_q[:, :arr.shape[1]])
+        np.testing.assert_array_equal(s, want_s)
+
+
+def test_q8_error_bound_and_extremes():
+    """|(float)q*s - v| <= s/2 (plus the product's own rounding); each nonzero row
+    reaches +-127 at its largest magnitude; codes keep the sign of v."""
+    rng = np.random.default_rng(5)
+    rows = (rng.standard_normal((64, 200)) *
+            np.exp(rng.uniform(-20, 20, size=(64, 1)))).astype(np.float32)
+    rows[3] = 0.0
+    rows[4, :] = 1e-30                       # tiny, denormal-free scale
+    q, s = oracle.quant_rows(rows)
+    deq = oracle.dequant_rows(q, s, "f32").astype(np.float64)
+    bound = s.astype(np.float64)[:, None] * (0.5 + 2.0 ** -20)
+    assert np.all(np.abs(deq - rows) <= bound)
+    for r in range(64):
+        if s[r] == 0:
+            assert not q[r].any()
+            continue
+        am = int(np.argmax(np.abs(rows[r])))
+        assert abs(int(q[r, am])) == 127
+    assert np.all((q == 0) | (np.sign(q) == np.sign(rows)))
+    assert np.abs(q.astype(np.int32)).max() <= 127
+
+
+def test_q8_skips_invalid_rows():
+    rows = np.ones((3, 8), np.float32)
+    q, s = oracle.quant_rows(rows, valid=np.array([0, -1, 5], np.int32))
+    assert np.isnan(s[1]) and not q[1].any()
+    assert s[0] == s[2] == np.float32(1.0) / np.float32(127.0)
+
+
+def test_float_to_bf16_matches_torch():
+    """The oracle's fp32 -> bf16 rounding against torch's conversion (round to nearest
+    even), including exact ties and values just either side of them."""
+    rng = np.random.default_rng(6)
+    base = rng.standard_normal(4096).astype(np.float32) * 100
+    bits = base.view(np.uint32) & 0xffff0000
+    ties = (bits | 0x8000).view(np.float32)
+    below = (bits | 0x7fff).view(np.float32)
+    above = (bits | 0x8001).view(np.float32)
+    a = np.concatenate([base, ties, below, above, np.float32([0.0, -0.0, 1e-30, 3.4e38])])
+    np.testing.assert_array_equal(oracle.float_to_bf16(a), _bf16_bits(a))
+
+
+def test_q8_dequant_bf16_is_rounded_fp32_product():
+    rng = np.random.default_rng(7)
+    q = rng.integers(-127, 128, size=(16, 64)).astype(np.int8)
+    s = (rng.uniform(0.5, 2.0, 16) * 1e-2).astype(np.float32)
+    prod = q.astype(np.float32) * s[:, None]            # IEEE fp32 products
+    np.testing.assert_array_equal(oracle.dequant_rows(q, s, "bf16"), _bf16_bits(prod))
+
+
+def test_combine_q8_closed_form():
+    """Two kept choices whose payload codes are all 1 with scale s, weights 0.25 and
+    0.75: out = x + s exactly; a token with both choices dropped is out = x."""
+    N, d, k = 3, 16, 2
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((N, d)).astype(np.float32)
+    yq = np.ones((4, d), np.int8)
+    s = np.float32(0.125)
+    yscale = np.full(4, s, np.float32)
+    slot_of = np.array([[0, 1], [-1, -1], [3, 2]], np.int32)
+    w = np.array([[0.25, 0.75], [0.5, 0.5], [0.25, 0.75]])
+    out = oracle.combine_q8(np.arange(N, dtype=np.int32), x, yq, yscale, slot_of, w)
+    np.testing.assert_array_equal(out[0], x[0].astype(np.float64) + 0.125)
+    np.testing.assert_array_equal(out[1], x[1].astype(np.float64))
+    np.testing.assert_array_equal(out[2], x[2].astype(np.float64) + 0.125)
+    # a negative code enters with its sign, weighted by its own choice's weight
+    yq[3, :] = -2
+    out = oracle.combine_q8(np.arange(N, dtype=np.int32), x, yq, yscale, slot_of, w)
+    np.testing.assert_array_equal(out[2], x[2].astype(np.float64) + 0.75 * 0.125 - 0.25 * 0.25)
