@@ -549,7 +549,8 @@ int oracle_bias_update(int E, int N, int k, const int32_t* counts, float step, f
 // [BZ-D]: quantising the all-to-all payload to INT8 halves its traffic again.  The
 // pages fix no format; the reading taken (symmetric, one fp32 scale per row):
 //   s   = max_i |v_i| / 127                  fp32 divide
-//   q_i = rint(v_i / s), clamped to +-127     fp32 divide, round half to even
+//   r   = 1 / s                              fp32 divide, once per row
+//   q_i = rint(v_i * r), clamped to +-127     fp32 multiply, round half to even
 //   a row of zeros has s = 0 and q = 0
 // The receiver's value is (float)q_i * s, one fp32 multiply, rounded once to the
 // activation type.  A code is an integer decided in floating point, so it is decided
@@ -568,11 +569,12 @@ int oracle_quant_rows(int rows, int d, int act_dtype, const void* in, const int3
     }
     const float s = amax / 127.0f;
     scale[r] = s;
+    const float inv = s > 0.0f ? 1.0f / s : 0.0f;
     for (int i = 0; i < d; ++i) {
       int c = 0;
       if (s > 0.0f) {
         const float v = static_cast<float>(load_act(in, act_dtype, base + i));
-        const float ratio = v / s;
+        const float ratio = v * inv;
         c = static_cast<int>(std::nearbyint(ratio));  // default mode: nearest, ties even
         c = std::min(127, std::max(-127, c));
       }
