@@ -234,19 +234,7 @@ def capture_layer(moe, b, inp, bias_step, reduce, world):
         with torch.cuda.graph(g):
             moe.run_layer(b, inp, bias_step=bias_step)
         return g.replay
-    c, cb = b.cfg, moe.with_tokens(b.cfg, b.cfg.tokens * world)
-    parts = [
-        lambda: (moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"],
-                               b.logits, b.topk_idx, b.topk_w, b.workspace),
-                 moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts,
-                                  b.kept_counts, b.expert_start, b.rank_counts, b.rank_offsets,
-                                  b.slot_of, b.perm_src, b.num_kept, b.workspace)),
-        lambda: (moe.moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
-                                    inp["w_down"], inp["x"], inp["shared_gate_up"],
-                                    inp["shared_down"], b.yperm, b.yshared, b.workspace),
-                 moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out)),
-        lambda: moe.moe_bias_update(cb, b.expert_counts, inp["sel_bias"], bias_step),
-    ]
+    parts = moe.layer_parts(b, inp, bias_step, replicas=world)
     graphs = []
     for f in parts:
         g = torch.cuda.CUDAGraph()
@@ -269,18 +257,30 @@ def launches_per_step(w):
     n += 2                     # expert FFN: gate_up and down grouped GEMMs
     n += 1                     # combine
     n += 1 if w.bias_step else 0
+    if getattr(w, "payload", "act") == "int8":
+        n += 2                 # receiver dequantisation, return-trip quantisation
     return n
 
 
 def algorithmic(w, num_kept):
-    """Bytes / flops the method must move or compute in one step."""
+    """Bytes the dispatch / combine side must move, the expert flops, and the bytes an
+    all-to-all would carry, for one step."""
     s = 2 if w.act_dtype == "bf16" else 4
     N, d = w.tokens, w.hidden
     ns = N if w.shared_d_ff else 0
-    dispatch_bytes = (N + num_kept) * d * s                 # read every token once, write kept rows
-    combine_bytes = (num_kept + N + ns + N) * d * s          # kept rows + residual + shared + out
     flops = 6.0 * d * (w.d_ff * num_kept + w.shared_d_ff * ns)
-    return dispatch_bytes, combine_bytes, flops
+    if getattr(w, "payload", "act") == "int8":
+        q = d + 4                                            # codes + fp32 scale per row
+        dispatch_bytes = N * d * s + num_kept * q            # read tokens, write codes
+        dispatch_bytes += num_kept * (q + d * s)             # receiver: codes -> rows
+        combine_bytes = num_kept * (d * s + q)               # expert rows -> codes
+        combine_bytes += num_kept * q + (N + ns + N) * d * s  # codes + residual + shared + out
+        wire = 2 * num_kept * q
+    else:
+        dispatch_bytes = (N + num_kept) * d * s              # read every token once, write kept rows
+        combine_bytes = (num_kept + N + ns + N) * d * s      # kept rows + residual + shared + out
+        wire = 2 * num_kept * d * s
+    return dict(dispatch=dispatch_bytes, combine=combine_bytes, flops=flops, wire=wire)
 
 
 def run_native(a, w, rank, world, local):
@@ -299,24 +299,41 @@ def run_native(a, w, rank, world, local):
     s = torch.cuda.current_stream()
 
     c = b.cfg
-    stages = [
-        lambda: moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"],
-                              b.logits, b.topk_idx, b.topk_w, b.workspace),
-        lambda: moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts,
-                                 b.kept_counts, b.expert_start, b.rank_counts, b.rank_offsets,
-                                 b.slot_of, b.perm_src, b.num_kept, b.workspace),
-        lambda: moe.moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
-                                   inp["w_down"], inp["x"], inp["shared_gate_up"],
-                                   inp["shared_down"], b.yperm, b.yshared, b.workspace),
-        lambda: moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out),
-    ]
+    # (name, C-ABI call) in path order; the INT8-payload path sends and returns codes
+    stages = [("route", lambda: moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"],
+                                              inp["sel_bias"], b.logits, b.topk_idx, b.topk_w,
+                                              b.workspace))]
+    if b.int8_payload:
+        stages += [
+            ("dispatch", lambda: moe.moe_dispatch_q8(
+                c, b.topk_idx, inp["x"], b.xperm_q, b.xscale, b.expert_counts, b.kept_counts,
+                b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
+                b.num_kept, b.workspace)),
+            ("dequant", lambda: moe.moe_dequant_rows(c, b.xperm_q, b.xscale, b.perm_src,
+                                                     b.xperm))]
+    else:
+        stages.append(("dispatch", lambda: moe.moe_dispatch(
+            c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts, b.expert_start,
+            b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src, b.num_kept, b.workspace)))
+    stages.append(("expert_ffn", lambda: moe.moe_expert_ffn(
+        c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"], inp["w_down"], inp["x"],
+        inp["shared_gate_up"], inp["shared_down"], b.yperm, b.yshared, b.workspace)))
+    if b.int8_payload:
+        stages += [
+            ("quant", lambda: moe.moe_quant_rows(c, b.yperm, b.perm_src, b.yperm_q, b.yscale)),
+            ("combine", lambda: moe.moe_combine_q8(c, b.yperm_q, b.yscale, b.slot_of, b.topk_w,
+                                                   inp["x"], b.yshared, b.out))]
+    else:
+        stages.append(("combine", lambda: moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w,
+                                                          inp["x"], b.yshared, b.out)))
     has_bias = bool(step_bias) and inp["sel_bias"] is not None
     # the bias update applies the sign rule to the routed counts of all replicas
     reduce = counts_allreduce(world) if has_bias else None
     cb = moe.with_tokens(c, w.tokens * world) if world > 1 else c
     if has_bias:
-        stages.append(lambda: moe.moe_bias_update(cb, b.expert_counts, inp["sel_bias"],
-                                                  step_bias))
+        stages.append(("bias_update", lambda: moe.moe_bias_update(cb, b.expert_counts,
+                                                                  inp["sel_bias"], step_bias)))
+    names = [n for n, _ in stages]
     n_st = len(stages)
 
     def step(runs, evs=None):
@@ -324,16 +341,17 @@ def run_native(a, w, rank, world, local):
         if evs is not None:
             evs[0].record(s)
         for j, r in enumerate(runs):
-            if j == 4 and h is not None:
+            if names[j] == "bias_update" and h is not None:
                 h.wait()              # the summed counts feed the bias update
             r()
-            if j == 1 and reduce is not None:
+            if names[j] == "dispatch" and reduce is not None:
                 h = reduce(b.expert_counts)   # overlaps the expert FFN and combine
             if evs is not None:
                 evs[j + 1].record(s)
 
+    calls = [f for _, f in stages]
     for _ in range(a.warmup):
-        step(stages)
+        step(calls)
     torch.cuda.synchronize()
     if bias0 is not None:
         inp["sel_bias"].copy_(bias0)
@@ -342,10 +360,10 @@ def run_native(a, w, rank, world, local):
 
     # each C-ABI call captured as its own CUDA graph, so that events between the graph
     # launches time every stage inside the timed region
-    runs = stages
+    runs = calls
     if not a.no_graph:
         runs = []
-        for f in stages:
+        for f in calls:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 f()
@@ -373,8 +391,10 @@ def run_native(a, w, rank, world, local):
     step_ms = per.sum(axis=1)
     total_s = max_over_ranks(step_ms.sum() / 1e3, world)
     value = weak_scaling_value(w.tokens, a.steps, world, total_s)
-    route_ms, disp_ms, ffn_ms, comb_ms = per.mean(axis=0)[:4]
-    bias_ms = float(per.mean(axis=0)[4]) if n_st > 4 else 0.0
+    stage_ms = {n: float(v) for n, v in zip(names, per.mean(axis=0))}
+    ffn_ms = stage_ms["expert_ffn"]
+    # every stage on the dispatch / combine side of the expert FFN
+    dc_ms = sum(v for n, v in stage_ms.items() if n in ("dispatch", "dequant", "quant", "combine"))
     status = int(b.workspace[:4].view(torch.int32).item())
     if bias0 is not None:
         inp["sel_bias"].copy_(bias0)
@@ -452,11 +472,12 @@ def run_native(a, w, rank, world, local):
 
     # ---------------- roofline figures
     pk = peaks()
-    disp_b, comb_b, flops = algorithmic(w, num_kept)
+    alg = algorithmic(w, num_kept)
+    flops = alg["flops"]
     ffn_tflops = flops / (ffn_ms * 1e-3) / 1e12
-    # dispatch+combine: bytes over (permute + combine) time; the dispatch call also
-    # holds the count / scan / assign kernels, included here (conservative)
-    dc_gbs = (disp_b + comb_b) / ((disp_ms + comb_ms) * 1e-3) / 1e9
+    # dispatch+combine: bytes over the time of every call on that side; the dispatch
+    # call also holds the count / scan / assign kernels, included here (conservative)
+    dc_gbs = (alg["dispatch"] + alg["combine"]) / (dc_ms * 1e-3) / 1e9
     out = {
         "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": float(step_ms.mean()),
@@ -468,7 +489,9 @@ def run_native(a, w, rank, world, local):
                    "capacity_factor": w.capacity_factor, "seed": a.seed,
                    "l2": "flushed between steps (252 MiB write outside the step events); "
                          "per-step working set larger than L2",
-                   "parallelism": f"replica x{world} (token-sharded, no collective)",
+                   "parallelism": f"replica x{world} (token-sharded; forward path without "
+                                  "collectives; with several replicas one [E] int32 all-reduce "
+                                  "of expert_counts feeds the bias update)",
                    "launch": "one CUDA graph per C-ABI call" if not a.no_graph
                              else "direct C-ABI calls"},
         "roofline": {"kernel": "expert grouped GEMMs (gate_up+SwiGLU, down) of moe_expert_ffn",
@@ -480,12 +503,12 @@ def run_native(a, w, rank, world, local):
                      "traffic": (measured_ffn_traffic() if w.name == "dsv3_prefill" else None),
                      "traffic_unit": "bytes per moe_expert_ffn call (ncu dram read+write)",
                      "algorithmic_flops_per_launch": flops},
-        "dispatch_combine": {"bytes": disp_b + comb_b, "achieved": dc_gbs, "unit": "GB/s",
-                             "peak": pk["hbm"], "frac": dc_gbs / pk["hbm"],
-                             "frac_of_8TBs": dc_gbs / 8000.0},
-        "stage_ms": {"route": route_ms, "dispatch": disp_ms, "expert_ffn": ffn_ms,
-                     "combine": comb_ms, "bias_update": bias_ms,
-                     "note": "events between the calls of each timed step"},
+        "dispatch_combine": {"bytes": alg["dispatch"] + alg["combine"], "achieved": dc_gbs,
+                             "unit": "GB/s", "peak": pk["hbm"], "frac": dc_gbs / pk["hbm"],
+                             "frac_of_8TBs": dc_gbs / 8000.0,
+                             "payload": getattr(w, "payload", "act"),
+                             "all_to_all_bytes_per_step": alg["wire"]},
+        "stage_ms": dict(stage_ms, note="events between the calls of each timed step"),
         "routing": {"num_kept": num_kept, "drop_rate": 1.0 - num_kept / (w.tokens * w.top_k)},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                 "d2h_bytes_per_step": io_bytes,
@@ -494,7 +517,9 @@ def run_native(a, w, rank, world, local):
         "clocks": clocks, "gpu_launches": launches_per_step(w) * a.steps,
         "device_status": status,
     }
-    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+    if getattr(w, "payload", "act") == "int8":
+        out["cpu_baseline"] = None           # the oracle baseline times the bf16-payload layer
+    elif rank == 0 and world == 1 and not a.no_cpu_baseline:
         del b, flush
         torch.cuda.empty_cache()
         out["cpu_baseline"] = cpu_baseline(w, oracle_inputs(inp))

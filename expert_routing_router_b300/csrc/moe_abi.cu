@@ -326,6 +326,75 @@ moe_status moe_bias_update(const moe_config* cfg, const int32_t* expert_counts, 
                                       static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_dispatch_q8(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                           int8_t* xperm_q, float* xscale, int32_t* expert_counts,
+                           int32_t* kept_counts, int32_t* expert_start, int32_t* rank_counts,
+                           int32_t* rank_offsets, int32_t* slot_of, int32_t* perm_src,
+                           int32_t* num_kept, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!topk_idx || !x || !xperm_q || !xscale || !expert_counts || !kept_counts ||
+      !expert_start || !rank_counts || !rank_offsets || !slot_of || !perm_src || !num_kept)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xperm_q, 16)) return MOE_ERR_INVALID_ARG;
+  const void* ints[] = {topk_idx, xscale, expert_counts, kept_counts, expert_start, rank_counts,
+                        rank_offsets, slot_of, perm_src, num_kept};
+  for (const void* p : ints)
+    if (!aligned(p, 4)) return MOE_ERR_INVALID_ARG;
+  WsLayout w;
+  if ((st = ws_check(c, workspace, workspace_bytes, &w)) != MOE_OK) return st;
+  if ((st = check_device()) != MOE_OK) return st;
+  int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + w.chunk_hist);
+  return from_cuda(launch_dispatch_q8(c, topk_idx, x, xperm_q, xscale, expert_counts, kept_counts,
+                                      expert_start, rank_counts, rank_offsets, slot_of, perm_src,
+                                      num_kept, hist, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quant_rows(const moe_config* cfg, const void* rows, const int32_t* perm_src,
+                          int8_t* q, float* scale, void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!rows || !perm_src || !q || !scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(rows, 16) || !aligned(q, 16) || !aligned(perm_src, 4) || !aligned(scale, 4))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  return from_cuda(launch_quant_rows(c, rows, perm_src, q, scale,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dequant_rows(const moe_config* cfg, const int8_t* q, const float* scale,
+                            const int32_t* perm_src, void* rows, void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!rows || !perm_src || !q || !scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(rows, 16) || !aligned(q, 16) || !aligned(perm_src, 4) || !aligned(scale, 4))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  return from_cuda(launch_dequant_rows(c, q, scale, perm_src, rows,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_q8(const moe_config* cfg, const int8_t* yperm_q, const float* yscale,
+                          const int32_t* slot_of, const float* topk_w, const void* residual,
+                          const void* yshared, void* out, void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!yperm_q || !yscale || !slot_of || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(yperm_q, 16) || !aligned(out, 16) || !aligned(yscale, 4) || !aligned(slot_of, 4) ||
+      !aligned(topk_w, 4))
+    return MOE_ERR_INVALID_ARG;
+  if ((residual && !aligned(residual, 16)) || (yshared && !aligned(yshared, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  return from_cuda(launch_combine_q8(c, yperm_q, yscale, slot_of, topk_w, residual, yshared, out,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "MOE_OK: success";

@@ -119,5 +119,18 @@ cudaError_t launch_combine(const Cfg& c, const void* yperm, const int32_t* slot_
                            void* out, cudaStream_t s);
 cudaError_t launch_bias_update(const Cfg& c, const int32_t* expert_counts, float* sel_bias,
                                float step, cudaStream_t s);
+// INT8 payload (payload_q8.cu)
+cudaError_t launch_dispatch_q8(const Cfg& c, const int32_t* topk_idx, const void* x, int8_t* xq,
+                               float* xscale, int32_t* expert_counts, int32_t* kept_counts,
+                               int32_t* expert_start, int32_t* rank_counts, int32_t* rank_offsets,
+                               int32_t* slot_of, int32_t* perm_src, int32_t* num_kept,
+                               int32_t* chunk_hist, cudaStream_t s);
+cudaError_t launch_quant_rows(const Cfg& c, const void* in, const int32_t* perm_src, int8_t* q,
+                              float* scale, cudaStream_t s);
+cudaError_t launch_dequant_rows(const Cfg& c, const int8_t* q, const float* scale,
+                                const int32_t* perm_src, void* out, cudaStream_t s);
+cudaError_t launch_combine_q8(const Cfg& c, const int8_t* yq, const float* yscale,
+                              const int32_t* slot_of, const float* topk_w, const void* residual,
+                              const void* yshared, void* out, cudaStream_t s);
 int num_sms();
 }  // namespace moe

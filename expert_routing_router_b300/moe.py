@@ -37,6 +37,7 @@ class MoeError(RuntimeError):
 
 EXPORTS = ("moe_send_rows", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc",
            "moe_expert_ffn", "moe_selftest_ffn_stall", "moe_combine", "moe_bias_update",
+           "moe_dispatch_q8", "moe_quant_rows", "moe_dequant_rows", "moe_combine_q8",
            "moe_status_string")
 
 
@@ -56,6 +57,10 @@ def _load():
     lib.moe_selftest_ffn_stall.argtypes = [C] + [P] * 11 + [S, P]
     lib.moe_combine.argtypes = [C] + [P] * 6 + [P]
     lib.moe_bias_update.argtypes = [C, P, P, F, P]
+    lib.moe_dispatch_q8.argtypes = [C] + [P] * 13 + [S, P]
+    lib.moe_quant_rows.argtypes = [C] + [P] * 4 + [P]
+    lib.moe_dequant_rows.argtypes = [C] + [P] * 4 + [P]
+    lib.moe_combine_q8.argtypes = [C] + [P] * 7 + [P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for fn in EXPORTS[:-1]:
@@ -167,6 +172,31 @@ def moe_bias_update(cfg, expert_counts, sel_bias, step, stream=None):
         ctypes.byref(cfg), _p(expert_counts), _p(sel_bias), float(step), _stream(stream)))
 
 
+def moe_dispatch_q8(cfg, topk_idx, x, xperm_q, xscale, expert_counts, kept_counts, expert_start,
+                    rank_counts, rank_offsets, slot_of, perm_src, num_kept, workspace, stream=None):
+    _check("moe_dispatch_q8", _lib.moe_dispatch_q8(
+        ctypes.byref(cfg), _p(topk_idx), _p(x), _p(xperm_q), _p(xscale), _p(expert_counts),
+        _p(kept_counts), _p(expert_start), _p(rank_counts), _p(rank_offsets), _p(slot_of),
+        _p(perm_src), _p(num_kept), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_quant_rows(cfg, rows, perm_src, q, scale, stream=None):
+    _check("moe_quant_rows", _lib.moe_quant_rows(
+        ctypes.byref(cfg), _p(rows), _p(perm_src), _p(q), _p(scale), _stream(stream)))
+
+
+def moe_dequant_rows(cfg, q, scale, perm_src, rows, stream=None):
+    _check("moe_dequant_rows", _lib.moe_dequant_rows(
+        ctypes.byref(cfg), _p(q), _p(scale), _p(perm_src), _p(rows), _stream(stream)))
+
+
+def moe_combine_q8(cfg, yperm_q, yscale, slot_of, topk_w, residual, yshared, out, stream=None):
+    _check("moe_combine_q8", _lib.moe_combine_q8(
+        ctypes.byref(cfg), _p(yperm_q), _p(yscale), _p(slot_of), _p(topk_w), _p(residual),
+        _p(yshared), _p(out), _stream(stream)))
+
+
 class LayerBuffers:
     """Device buffers of one layer call, sized for the worst case (every assignment
     kept; the capacity-padded layout has E*C send rows)."""
@@ -192,6 +222,14 @@ class LayerBuffers:
         self.slot_of = torch.empty(N * k, **i32)
         self.perm_src = torch.empty(S, **i32)
         self.num_kept = torch.empty(1, **i32)
+        # INT8 payload path: send and return buffers as codes + per-row scales
+        self.int8_payload = getattr(w, "payload", "act") == "int8"
+        self.xperm_q = self.xscale = self.yperm_q = self.yscale = None
+        if self.int8_payload:
+            self.xperm_q = torch.empty(S, d, dtype=torch.int8, device=device)
+            self.xscale = torch.empty(S, dtype=torch.float32, device=device)
+            self.yperm_q = torch.empty(S, d, dtype=torch.int8, device=device)
+            self.yscale = torch.empty(S, dtype=torch.float32, device=device)
         nbytes = moe_workspace_size(self.cfg)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.workspace[:256].zero_()          # sticky device status word starts at 0
@@ -205,9 +243,52 @@ def with_tokens(cfg, tokens):
     return c
 
 
+def layer_parts(b, inp, bias_step=0.0, stream=None, replicas=1):
+    """The layer step as three stream-ordered parts: (1) route and dispatch, (2) expert
+    FFN and combine, (3) the bias update (None when there is none).  With an INT8
+    payload (LayerBuffers of a workload with payload="int8") the send and return
+    buffers hold INT8 codes + per-row scales: part 1 is route, dispatch_q8 and
+    dequant_rows; part 2 expert FFN, quant_rows and combine_q8.  With data-parallel
+    replicas the counts all-reduce goes between part 1 and part 3, and part 3 compares
+    the summed counts with the mean load of all `replicas` batches."""
+    c = b.cfg
+
+    def send():
+        moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"], b.logits,
+                  b.topk_idx, b.topk_w, b.workspace, stream)
+        if b.int8_payload:
+            moe_dispatch_q8(c, b.topk_idx, inp["x"], b.xperm_q, b.xscale, b.expert_counts,
+                            b.kept_counts, b.expert_start, b.rank_counts, b.rank_offsets,
+                            b.slot_of, b.perm_src, b.num_kept, b.workspace, stream)
+            moe_dequant_rows(c, b.xperm_q, b.xscale, b.perm_src, b.xperm, stream)
+        else:
+            moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
+                         b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
+                         b.num_kept, b.workspace, stream)
+
+    def compute_return():
+        moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
+                       inp["w_down"], inp["x"], inp["shared_gate_up"], inp["shared_down"],
+                       b.yperm, b.yshared, b.workspace, stream)
+        if b.int8_payload:
+            moe_quant_rows(c, b.yperm, b.perm_src, b.yperm_q, b.yscale, stream)
+            moe_combine_q8(c, b.yperm_q, b.yscale, b.slot_of, b.topk_w, inp["x"], b.yshared,
+                           b.out, stream)
+        else:
+            moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out, stream)
+
+    update = None
+    if bias_step and inp["sel_bias"] is not None:
+        cb = with_tokens(c, c.tokens * replicas) if replicas > 1 else c
+
+        def update():
+            moe_bias_update(cb, b.expert_counts, inp["sel_bias"], bias_step, stream)
+    return send, compute_return, update
+
+
 def run_layer(b, inp, bias_step=0.0, stream=None, reduce_counts=None, replicas=1):
     """One pass of the layer path through the C ABI: route, dispatch, expert FFN,
-    combine, and (if bias_step) the selection-bias update.
+    combine, and (if bias_step) the selection-bias update (see layer_parts).
 
     Data-parallel replicas (each its own token batch, the same layer): the bias update
     needs the load of every replica's batch.  `reduce_counts(expert_counts)` sums the
@@ -215,31 +296,22 @@ def run_layer(b, inp, bias_step=0.0, stream=None, reduce_counts=None, replicas=1
     whose .wait() orders it before the bias update, so that it overlaps the expert
     FFN), and the sign rule then compares the summed counts with the mean load of all
     `replicas` batches.  b.expert_counts holds the summed counts afterwards."""
-    c = b.cfg
-    moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"], b.logits,
-              b.topk_idx, b.topk_w, b.workspace, stream)
-    moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
-                 b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
-                 b.num_kept, b.workspace, stream)
-    update = bool(bias_step) and inp["sel_bias"] is not None
+    send, compute_return, update = layer_parts(b, inp, bias_step, stream, replicas)
+    send()
     handle = None
-    if update and reduce_counts is not None:
+    if update is not None and reduce_counts is not None:
         if stream is None:
             handle = reduce_counts(b.expert_counts)
         else:
             with torch.cuda.stream(stream):
                 handle = reduce_counts(b.expert_counts)
-    moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"], inp["w_down"],
-                   inp["x"], inp["shared_gate_up"], inp["shared_down"], b.yperm, b.yshared,
-                   b.workspace, stream)
-    moe_combine(c, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out, stream)
-    if update:
+    compute_return()
+    if update is not None:
         if handle is not None:
             if stream is None:
                 handle.wait()
             else:
                 with torch.cuda.stream(stream):
                     handle.wait()
-        cb = with_tokens(c, c.tokens * replicas) if replicas > 1 else c
-        moe_bias_update(cb, b.expert_counts, inp["sel_bias"], bias_step, stream)
+        update()
     return b.out

@@ -20,6 +20,8 @@ Workloads (named by what they are):
                       assigned round-robin.
   gshard_top2_padded  the GShard-shaped layer with the capacity-padded [E, C] send
                       buffer and choice-major capacity priority.
+  dsv3_prefill_int8   the DeepSeek-V3 prefill layer with the all-to-all payload (send
+                      and return buffers) as INT8 codes + per-row fp32 scales.
 """
 from dataclasses import dataclass, replace
 import math
@@ -54,6 +56,7 @@ class Workload:
     bias_step: float          # bias-update step (0 = no update in the step)
     expert_std: float = 0.02
     dispatch_mode: int = 0    # 0 packed token-order capacity, 1 capacity-padded choice-major
+    payload: str = "act"      # all-to-all payload: "act" (activation dtype) or "int8"
 
     def with_tokens(self, n):
         return replace(self, tokens=n, name=f"{self.name.split('@')[0]}@{n}")
@@ -72,12 +75,13 @@ GSHARD_TOP2 = Workload("gshard_top2_skewed", 32768, 2048, 64, 2, 16, RANK_CONTIG
 GSHARD_TOP2_PADDED = replace(GSHARD_TOP2, name="gshard_top2_padded", dispatch_mode=1)
 DSV3_PREFILL = Workload("dsv3_prefill", 8192, 7168, 256, 8, 64, RANK_CONTIGUOUS, SCORE_SIGMOID,
                         True, 8, 4, 0.0, 2048, 2048, "bf16", 0.0, 0.1, 1e-3)
+DSV3_PREFILL_INT8 = replace(DSV3_PREFILL, name="dsv3_prefill_int8", payload="int8")
 DSV3_DECODE = replace(DSV3_PREFILL, name="dsv3_decode", tokens=512, num_ranks=40,
                       rank_map=RANK_ROUND_ROBIN)
 DECODE_TOKENS = (1, 8, 64, 128, 512)
 
 WORKLOADS = {w.name: w for w in (TINY_TOP2_F32, SWITCH_TOP1, GSHARD_TOP2, GSHARD_TOP2_PADDED,
-                                 DSV3_PREFILL, DSV3_DECODE)}
+                                 DSV3_PREFILL, DSV3_PREFILL_INT8, DSV3_DECODE)}
 
 
 def _normal_(t, std, gen, chunk_rows=64):

@@ -244,6 +244,59 @@ MOE_API moe_status moe_combine(const moe_config* cfg, const void* yperm, const i
 MOE_API moe_status moe_bias_update(const moe_config* cfg, const int32_t* expert_counts, float* sel_bias,
                            float step, void* stream);
 
+/* ---- INT8 all-to-all payload ------------------------------------------------
+ * bowenzhou.top note "专家并行", section "深入推导：all-to-all 通信模型与 DeepSeek-V3
+ * 的 EP 配置" (DeepSeek-V3's two-level EP): INT8-quantised communication halves the
+ * all-to-all traffic again.  The pages fix no format; this library's format is
+ * symmetric with one fp32 scale per row:
+ *   s   = max_i |v_i| / 127                (fp32 divide)
+ *   r   = 1 / s                            (fp32 divide, once per row)
+ *   q_i = rint(v_i * r), clamped to +-127   (fp32 multiply, round half to even)
+ *   a row of zeros has s = 0 and all q = 0
+ *   received value = (float)q_i * s         (one fp32 multiply, then rounded once to
+ *                                           act_dtype)
+ * A row then travels as `hidden` int8 bytes plus one fp32 scale.  Rows must be
+ * finite.  The four calls below replace moe_dispatch's permute and moe_combine on a
+ * path whose send and return buffers hold this format:
+ *   moe_dispatch_q8 -> moe_dequant_rows -> moe_expert_ffn -> moe_quant_rows ->
+ *   moe_combine_q8.
+ * Send-buffer rows: S = moe_send_rows(cfg); a row holds an assignment iff
+ * perm_src[row] >= 0 (from moe_dispatch_q8); rows with perm_src < 0 are neither read
+ * nor written. */
+
+/* moe_dispatch with an INT8 send buffer: the same counts, capacity and slot tables
+ * (every int32 output identical to moe_dispatch's), and instead of xperm
+ *   xperm_q [S, hidden] int8   codes of the kept tokens' rows, 16-byte aligned
+ *   xscale  [S]         fp32   their scales
+ * Each token row is quantised once and written to every slot it was kept in. */
+MOE_API moe_status moe_dispatch_q8(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                                   int8_t* xperm_q, float* xscale, int32_t* expert_counts,
+                                   int32_t* kept_counts, int32_t* expert_start,
+                                   int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
+                                   int32_t* perm_src, int32_t* num_kept, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* Quantise the send-buffer rows that hold an assignment (the expert side of the
+ * return trip): rows [S, hidden] act_dtype -> q [S, hidden] int8 (16-byte aligned),
+ * scale [S] fp32. */
+MOE_API moe_status moe_quant_rows(const moe_config* cfg, const void* rows, const int32_t* perm_src,
+                                  int8_t* q, float* scale, void* stream);
+
+/* Receiver side: rows[r, i] = (float)q[r, i] * scale[r], stored as act_dtype, for the
+ * send-buffer rows that hold an assignment.  q [S, hidden] int8, scale [S] fp32,
+ * rows [S, hidden] act_dtype (16-byte aligned). */
+MOE_API moe_status moe_dequant_rows(const moe_config* cfg, const int8_t* q, const float* scale,
+                                    const int32_t* perm_src, void* rows, void* stream);
+
+/* moe_combine reading an INT8 return payload: expert output element = (float)q * s
+ * of its slot's row (fp32 multiply), then the same fp32 sum as moe_combine:
+ *   out[t] = residual[t] + yshared[t] + sum_{j kept, ascending} topk_w[t,j] * y_j.
+ * yperm_q [S, hidden] int8 (16-byte aligned), yscale [S] fp32; the other arguments as
+ * in moe_combine. */
+MOE_API moe_status moe_combine_q8(const moe_config* cfg, const int8_t* yperm_q, const float* yscale,
+                                  const int32_t* slot_of, const float* topk_w, const void* residual,
+                                  const void* yshared, void* out, void* stream);
+
 /* Static, NUL-terminated description of a status code (host pointer). */
 MOE_API const char* moe_status_string(moe_status status);
 

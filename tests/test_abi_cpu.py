@@ -111,3 +111,32 @@ def test_null_misaligned_and_small_workspace(moe_lib):
         moe_lib.MOE_ERR_INVALID_ARG
     assert moe_lib.lib.moe_combine(None, P(FAKE), P(FAKE), P(FAKE), None, None, P(FAKE),
                                    None) == moe_lib.MOE_ERR_INVALID_ARG
+
+
+def test_int8_payload_calls_validate_on_host(moe_lib):
+    """The INT8 payload calls reject null and misaligned buffers before any launch."""
+    P = ctypes.c_void_p
+    cfg = moe_lib.config(W.DSV3_PREFILL_INT8)
+    need = moe_lib.moe_workspace_size(cfg)
+    L = moe_lib.lib
+    # dispatch_q8: missing codes buffer, misaligned codes buffer, small workspace
+    assert L.moe_dispatch_q8(ctypes.byref(cfg), P(FAKE), P(FAKE), None, P(FAKE),
+                             *[P(FAKE)] * 8, P(FAKE), need, None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch_q8(ctypes.byref(cfg), P(FAKE), P(FAKE), P(FAKE + 8), P(FAKE),
+                             *[P(FAKE)] * 8, P(FAKE), need, None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch_q8(ctypes.byref(cfg), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                             *[P(FAKE)] * 8, P(FAKE), need - 1, None) == moe_lib.MOE_ERR_WORKSPACE
+    # quant / dequant: null perm_src, misaligned rows, misaligned scale
+    assert L.moe_quant_rows(ctypes.byref(cfg), P(FAKE), None, P(FAKE), P(FAKE),
+                            None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_quant_rows(ctypes.byref(cfg), P(FAKE + 8), P(FAKE), P(FAKE), P(FAKE),
+                            None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_dequant_rows(ctypes.byref(cfg), P(FAKE), P(FAKE + 2), P(FAKE), P(FAKE),
+                              None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_dequant_rows(None, P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                              None) == moe_lib.MOE_ERR_INVALID_ARG
+    # combine_q8: missing scales, misaligned residual
+    assert L.moe_combine_q8(ctypes.byref(cfg), P(FAKE), None, P(FAKE), P(FAKE), P(FAKE), None,
+                            P(FAKE), None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_q8(ctypes.byref(cfg), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE + 4),
+                            None, P(FAKE), None) == moe_lib.MOE_ERR_INVALID_ARG

@@ -71,11 +71,8 @@ def host_weights(inp):
             for k in ("w_gate_up", "w_down", "shared_gate_up", "shared_down")}
 
 
-def check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=None):
-    """All per-step and end-to-end checks for one layer call."""
-    if hw is None:
-        hw = host_weights(inp)
-    rng = np.random.default_rng(seed)
+def check_route_dispatch(w, inp, b, rng, n_sample_tokens):
+    """Logits, routing and dispatch tables (shared by both payload paths)."""
     N, k, E = w.tokens, w.top_k, w.num_experts
     x_h = host(inp["x"])
     # ---- logits (sampled rows at full size)
@@ -101,9 +98,60 @@ def check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=
     nk = int(host(b.num_kept)[0])
     assert nk == d["num_kept"]
     assert host(b.expert_counts).sum() == N * k
-    # ---- send buffer rows are exact copies (the rows that hold an assignment)
     kept_rows = np.nonzero(d["perm_src"] >= 0)[0]
     assert kept_rows.size == nk
+    return x_h, idx_gpu, w_ref, d, nk, kept_rows
+
+
+def sample_tokens(rng, N, n_sample_tokens, d, k):
+    """Token sample (or all), always including fully dropped tokens (up to 32)."""
+    slot = d["slot_of"].reshape(N, k)
+    dropped = np.nonzero((slot < 0).all(axis=1))[0]
+    if n_sample_tokens is None:
+        toks = np.arange(N)
+    else:
+        toks = np.unique(np.concatenate([rng.choice(N, size=min(N, n_sample_tokens), replace=False),
+                                         dropped[:32]]))
+    return toks.astype(np.int32), dropped
+
+
+# relative rounding of one store to the output type (round to nearest: half an ulp,
+# taken as a full ulp to cover the last fp32 additions before the store)
+OUT_ROUNDING = {"f32": 2.0 ** -23, "bf16": 2.0 ** -8}
+
+
+def check_layer_output(w, out_got, x_h, toks, l_ref):
+    """The layer output, and the MoE delta (out - x), against the oracle's layer.  The
+    delta gate keeps an FFN error from hiding behind the residual: elementwise
+    |got - ref| <= tol * max|delta_ref| + (output rounding) * |out_ref|, the second
+    term being the storage rounding of out itself, which a small delta cannot absorb."""
+    rel = close(out_got[toks], l_ref, TOL_OUT[w.act_dtype], "layer output")
+    xt = x_h[toks].astype(np.float64) if w.act_dtype == "f32" else bf16_to_f64(x_h[toks])
+    d_got, d_ref = out_got[toks] - xt, l_ref - xt
+    if d_ref.size:
+        allow = TOL_OUT[w.act_dtype] * np.max(np.abs(d_ref)) + \
+            OUT_ROUNDING[w.act_dtype] * np.abs(l_ref)
+        bad = np.abs(d_got - d_ref) > allow
+        assert not bad.any(), (f"layer delta (out - x): {int(bad.sum())} elements off, worst "
+                               f"{np.max(np.abs(d_got - d_ref) - allow):.3e} beyond the allowance; "
+                               f"max|delta_ref| {np.max(np.abs(d_ref)):.3e}")
+    return rel
+
+
+def bf16_to_f64(a):
+    return (np.asarray(a, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=None):
+    """All per-step and end-to-end checks for one layer call."""
+    if getattr(w, "payload", "act") == "int8":
+        return check_layer_int8(w, inp, b, n_sample_tokens, n_sample_rows, seed, hw)
+    if hw is None:
+        hw = host_weights(inp)
+    rng = np.random.default_rng(seed)
+    N, k, E = w.tokens, w.top_k, w.num_experts
+    x_h, idx_gpu, w_ref, d, nk, kept_rows = check_route_dispatch(w, inp, b, rng, n_sample_tokens)
+    # ---- send buffer rows are exact copies (the rows that hold an assignment)
     ps = d["perm_src"][kept_rows]
     xp = host(b.xperm[torch.from_numpy(kept_rows).cuda().long()]) if nk else x_h[:0]
     np.testing.assert_array_equal(xp, x_h[ps // k], err_msg="xperm")
@@ -123,14 +171,7 @@ def check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=
         close(f64(b.yshared[torch.from_numpy(trows).cuda().long()]), ys_ref, TOL_OUT[w.act_dtype],
               "shared expert rows")
     # ---- combine from the GPU's yperm / weights, and the whole layer
-    slot = d["slot_of"].reshape(N, k)
-    dropped = np.nonzero((slot < 0).all(axis=1))[0]
-    if n_sample_tokens is None:
-        toks = np.arange(N)
-    else:
-        toks = np.unique(np.concatenate([rng.choice(N, size=min(N, n_sample_tokens), replace=False),
-                                         dropped[:32]]))
-    toks = toks.astype(np.int32)
+    toks, dropped = sample_tokens(rng, N, n_sample_tokens, d, k)
     ys_h = None if b.yshared is None else host(b.yshared)
     out_got = f64(b.out)
     c_ref = oracle.combine(toks, x_h, host(b.yperm), d["slot_of"],
@@ -140,7 +181,88 @@ def check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=
         # a token whose every choice was dropped leaves the layer unchanged, bit for bit
         np.testing.assert_array_equal(host(b.out)[dropped], x_h[dropped])
     l_ref = oracle.layer_tokens(toks, x_h, idx_gpu, w_ref, d["slot_of"], wgu, wd, sgu, sd)
-    rel = close(out_got[toks], l_ref, TOL_OUT[w.act_dtype], "layer output")
+    rel = check_layer_output(w, out_got, x_h, toks, l_ref)
+    return dict(rel_err=rel, drop_rate=1.0 - nk / (N * k), num_kept=nk)
+
+
+def check_layer_int8(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=None):
+    """The INT8-payload path, step by step:
+      send codes/scales   oracle quantisation of the kept tokens' rows     bit-exact
+      received rows       oracle dequantisation of the GPU's codes         bit-exact
+      expert FFN          oracle fp64 FFN of the GPU's received rows       as check_layer
+      return codes/scales oracle quantisation of the GPU's expert rows     bit-exact
+      combine             oracle fp64 sum of the GPU's return payload      one output rounding
+      layer               oracle layer with the routed experts fed the dequantised rows,
+                          expert outputs unquantised; the allowance adds one code step
+                          of the return payload per kept choice."""
+    if hw is None:
+        hw = host_weights(inp)
+    rng = np.random.default_rng(seed)
+    N, k, E = w.tokens, w.top_k, w.num_experts
+    x_h, idx_gpu, w_ref, d, nk, kept_rows = check_route_dispatch(w, inp, b, rng, n_sample_tokens)
+    ps = d["perm_src"][kept_rows]
+    sel = np.arange(nk) if n_sample_rows is None else np.sort(
+        rng.choice(nk, size=min(nk, n_sample_rows), replace=False))
+    rows = kept_rows[sel]
+    rows_t = torch.from_numpy(rows).cuda().long()
+    # ---- send payload: codes and scales of the kept tokens' rows
+    q_ref, s_ref = oracle.quant_rows(x_h[ps[sel] // k])
+    xq = b.xperm_q[rows_t].cpu().numpy()
+    np.testing.assert_array_equal(xq, q_ref, err_msg="send codes")
+    np.testing.assert_array_equal(b.xscale[rows_t].cpu().numpy(), s_ref, err_msg="send scales")
+    # ---- receiver: dequantised rows
+    xdq = host(b.xperm[rows_t])
+    np.testing.assert_array_equal(xdq, oracle.dequant_rows(xq, s_ref, w.act_dtype),
+                                  err_msg="received rows")
+    # ---- expert FFN on the received rows
+    flat_idx = idx_gpu.reshape(-1)
+    wgu, wd, sgu, sd = hw["w_gate_up"], hw["w_down"], hw["shared_gate_up"], hw["shared_down"]
+    if sel.size:
+        y_ref = oracle.expert_rows(xdq, flat_idx[ps[sel]], wgu, wd)
+        close(f64(b.yperm[rows_t]), y_ref, TOL_OUT[w.act_dtype], "expert FFN rows")
+        # ---- return payload: codes and scales of the GPU's expert rows
+        yq_ref, ys_ref = oracle.quant_rows(host(b.yperm[rows_t]))
+        np.testing.assert_array_equal(b.yperm_q[rows_t].cpu().numpy(), yq_ref,
+                                      err_msg="return codes")
+        np.testing.assert_array_equal(b.yscale[rows_t].cpu().numpy(), ys_ref,
+                                      err_msg="return scales")
+    # ---- combine from the GPU's return payload
+    toks, dropped = sample_tokens(rng, N, n_sample_tokens, d, k)
+    ys_h = None if b.yshared is None else host(b.yshared)
+    out_got = f64(b.out)
+    c_ref = oracle.combine_q8(toks, x_h, b.yperm_q.cpu().numpy(), b.yscale.cpu().numpy(),
+                              d["slot_of"], host(b.topk_w).astype(np.float64), ys_h)
+    close(out_got[toks], c_ref, TOL_COMBINE[w.act_dtype], "combine (INT8 payload)")
+    if w.shared_d_ff == 0 and dropped.size:
+        np.testing.assert_array_equal(host(b.out)[dropped], x_h[dropped])
+    # ---- layer: routed experts see the dequantised token rows; shared expert and
+    # residual see x itself (they never cross the all-to-all)
+    q_all, s_all = oracle.quant_rows(x_h[toks])
+    xdq_t = oracle.dequant_rows(q_all, s_all, w.act_dtype)
+    xdq_full = np.array(x_h, copy=True)
+    xdq_full[toks] = xdq_t
+    routed = oracle.layer_tokens(toks, xdq_full, idx_gpu, w_ref, d["slot_of"], wgu, wd)
+    xdq64 = xdq_t.astype(np.float64) if w.act_dtype == "f32" else bf16_to_f64(xdq_t)
+    xt64 = x_h[toks].astype(np.float64) if w.act_dtype == "f32" else bf16_to_f64(x_h[toks])
+    l_ref = xt64 + (routed - xdq64)
+    if sgu is not None:
+        l_ref += oracle.expert_rows(x_h[toks], np.full(toks.size, E, np.int32), wgu, wd, sgu, sd)
+    # The reference keeps the expert outputs unquantised.  The return trip moves each
+    # kept term by at most one code step of its row (half a step of rounding; one more
+    # where the GPU's and the oracle's y straddle a code boundary), so the allowance
+    # adds sum_j w_j * s_j per token (s_j: that row's scale) to the usual terms.
+    slot = d["slot_of"].reshape(N, k)[toks]
+    ysc = b.yscale.cpu().numpy()
+    wts = host(b.topk_w).astype(np.float64)[toks]
+    qstep = np.where(slot >= 0, wts * ysc[np.maximum(slot, 0)].astype(np.float64), 0.0).sum(1)
+    tol = TOL_OUT[w.act_dtype]
+    for what, got_v, ref_v in (("layer output", out_got[toks], l_ref),
+                               ("layer delta (out - x)", out_got[toks] - xt64, l_ref - xt64)):
+        allow = tol * np.max(np.abs(ref_v)) + qstep[:, None] + \
+            OUT_ROUNDING[w.act_dtype] * np.abs(l_ref)
+        bad = np.abs(got_v - ref_v) > allow
+        assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond the allowance"
+    rel = np.max(np.abs(out_got[toks] - l_ref)) / max(np.max(np.abs(l_ref)), 1e-300)
     return dict(rel_err=rel, drop_rate=1.0 - nk / (N * k), num_kept=nk)
 
 
@@ -337,3 +459,74 @@ def test_layer_replays_from_a_cuda_graph_bit_exactly():
         assert torch.equal(b.out, ref_out)
         assert torch.equal(inp["sel_bias"], ref_bias)
         assert int(b.workspace[:4].view(torch.int32).item()) == 0
+
+
+# ---------------------------------------------------------------- INT8 all-to-all payload
+
+INT8_EDGE = {
+    "int8_ragged_sigmoid_groups_shared": small(payload="int8"),
+    "int8_f32_softmax_cap": dataclasses.replace(EDGE["ragged_f32_softmax_cap"], payload="int8"),
+    "int8_padded_round_robin": dataclasses.replace(EDGE["padded_choice_major_round_robin"],
+                                                   payload="int8"),
+    "int8_minimal_sizes": dataclasses.replace(EDGE["minimal_sizes_bf16"], payload="int8"),
+    "int8_small_segments": dataclasses.replace(EDGE["small_segments_ragged"], payload="int8"),
+    # rows longer than the register-cached part (8192 bf16): the code pass re-reads them
+    "int8_long_rows": small(tokens=24, hidden=8200, num_experts=8, top_k=2, num_ranks=2,
+                            num_groups=1, topk_groups=1, d_ff=64, shared_d_ff=0,
+                            sel_bias_std=0.0, score_fn=0, payload="int8"),
+}
+
+
+@pytest.mark.parametrize("name", list(INT8_EDGE))
+def test_int8_payload_cases(name):
+    w = INT8_EDGE[name]
+    inp = W.make_inputs(w, seed=6, device="cuda")
+    b, _ = run_gpu(w, inp)
+    check_layer(w, inp, b)
+
+
+def test_int8_payload_zero_and_extreme_rows():
+    """An all-zero token row travels as scale 0 and zero codes; rows scaled by 1e-30
+    and 1e3 keep their relative precision (the scale follows the row)."""
+    w = INT8_EDGE["int8_ragged_sigmoid_groups_shared"]
+    inp = W.make_inputs(w, seed=7, device="cuda")
+    inp["x"][0] = 0
+    inp["x"][1] *= 1e-30
+    inp["x"][2] *= 1e3
+    b, _ = run_gpu(w, inp)
+    check_layer(w, inp, b)
+    slots = host(b.slot_of).reshape(w.tokens, w.top_k)[0]
+    for s in slots[slots >= 0]:
+        assert float(b.xscale[int(s)]) == 0.0
+        assert not b.xperm_q[int(s)].any()
+
+
+def test_dsv3_prefill_int8_payload(dsv3_inputs):
+    w, (inp, hw) = W.DSV3_PREFILL_INT8, dsv3_inputs
+    b, bias0 = run_gpu(w, inp)
+    check_layer(w, inp, b, n_sample_tokens=48, n_sample_rows=128, hw=hw)
+    if bias0 is not None:
+        inp["sel_bias"].copy_(bias0)
+    del b
+    torch.cuda.empty_cache()
+
+
+def test_int8_payload_graph_replay_bit_exact():
+    from expert_routing_router_b300 import moe
+    w = INT8_EDGE["int8_ragged_sigmoid_groups_shared"]
+    inp = W.make_inputs(w, seed=8, device="cuda")
+    bias0 = inp["sel_bias"].clone()
+    b = moe.LayerBuffers(w)
+    moe.run_layer(b, inp, bias_step=w.bias_step)
+    torch.cuda.synchronize()
+    ref_out, ref_bias = b.out.clone(), inp["sel_bias"].clone()
+    inp["sel_bias"].copy_(bias0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.run_layer(b, inp, bias_step=w.bias_step)
+    inp["sel_bias"].copy_(bias0)
+    b.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(b.out, ref_out)
+    assert torch.equal(inp["sel_bias"], ref_bias)
