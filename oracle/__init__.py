@@ -47,6 +47,12 @@ def _lib():
         lib.oracle_dequant_rows.argtypes = [I, I, I, P, P, P, P]
         lib.oracle_combine_q8.argtypes = [I, P, I, I, I, P, P, P, P, P, P, P]
         lib.oracle_float_to_bf16.argtypes = [ctypes.c_int64, P, P]
+        lib.oracle_combine_backward.argtypes = [I, I, I, I, P, P, P, P, P, P]
+        lib.oracle_ffn_backward_rows.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P]
+        lib.oracle_ffn_wgrad.argtypes = [I, I, I, I, P, P, P, P, I, P, P, P, P]
+        lib.oracle_route_backward.argtypes = [I, I, I, I, I, P, P, P, P]
+        lib.oracle_router_grads.argtypes = [I, I, I, I, P, P, P, I, P, P, P, P]
+        lib.oracle_dispatch_backward.argtypes = [I, P, I, I, I, P, P, P, P, P, P]
         _LIB = lib
     return _LIB
 
@@ -255,4 +261,110 @@ def float_to_bf16(a):
     a = np.ascontiguousarray(a, dtype=np.float32)
     out = np.empty(a.shape, np.uint16)
     _lib().oracle_float_to_bf16(a.size, _p(a), _p(out))
+    return out
+
+
+# ------------------------------------------------------------------ backward
+
+def combine_backward(dout, yperm, slot_of, w):
+    """dy [S, d] fp64 (written at kept slots, 0 elsewhere) and dw [N, k] fp64."""
+    dout, code = _act(dout)
+    yperm, c2 = _act(yperm)
+    assert code == c2
+    N, d = dout.shape
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32).reshape(-1)
+    k = slot_of.size // N
+    w = np.ascontiguousarray(w, dtype=np.float64).reshape(-1)
+    dy = np.zeros((yperm.shape[0], d), np.float64)
+    dw = np.empty(N * k, np.float64)
+    _lib().oracle_combine_backward(N, d, k, code, _p(dout), _p(yperm), _p(slot_of), _p(w),
+                                   _p(dy), _p(dw))
+    return dy, dw.reshape(N, k)
+
+
+def ffn_backward_rows(xrows, dyrows, expert, w_gate_up, w_down, shared_gate_up=None,
+                      shared_down=None):
+    """dx [n, d] fp64 of each row through its expert (expert id E = the shared expert)."""
+    xrows, code = _act(xrows)
+    dyrows, c1 = _act(dyrows)
+    assert code == c1
+    wgu, _ = _act(w_gate_up)
+    wd, _ = _act(w_down)
+    n, d = xrows.shape
+    E, twoF, _ = wgu.shape
+    sgu = sd = None
+    Fs = 0
+    if shared_gate_up is not None:
+        sgu, _ = _act(shared_gate_up)
+        sd, _ = _act(shared_down)
+        Fs = sgu.shape[0] // 2
+    expert = np.ascontiguousarray(expert, dtype=np.int32)
+    dx = np.empty((n, d), np.float64)
+    _lib().oracle_ffn_backward_rows(n, d, E, twoF // 2, Fs, code, _p(xrows), _p(dyrows),
+                                    _p(expert), _p(wgu), _p(wd), _p(sgu), _p(sd), _p(dx))
+    return dx
+
+
+def ffn_wgrad(xrows, dyrows, wgu_e, wd_e, fs=None):
+    """Weight gradients of one expert from its rows: for each hidden unit f in fs
+    (default all), dWd[:, f], dWg[f, :], dWu[f, :] as three [nf, d] fp64 arrays."""
+    xrows, code = _act(xrows)
+    dyrows, c1 = _act(dyrows)
+    assert code == c1
+    wgu_e, _ = _act(wgu_e)
+    wd_e, _ = _act(wd_e)
+    n, d = xrows.shape
+    Fx = wgu_e.shape[0] // 2
+    fs = np.arange(Fx, dtype=np.int32) if fs is None else np.ascontiguousarray(fs, np.int32)
+    nf = fs.size
+    out = [np.empty((nf, d), np.float64) for _ in range(3)]
+    _lib().oracle_ffn_wgrad(n, d, Fx, code, _p(xrows), _p(dyrows), _p(wgu_e), _p(wd_e), nf, _p(fs),
+                            *[_p(o) for o in out])
+    return out
+
+
+def route_backward(logits, idx, dw, score_fn=0, normalize=True):
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    N, E = logits.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    k = idx.shape[1]
+    dw = np.ascontiguousarray(dw, dtype=np.float64)
+    dl = np.empty((N, E), np.float64)
+    _lib().oracle_route_backward(N, E, k, score_fn, int(bool(normalize)), _p(logits), _p(idx),
+                                 _p(dw), _p(dl))
+    return dl
+
+
+def router_grads(x, w_router, dl, tokens=None, params=True):
+    """(dx_router [ntok, d], dWr [E, d] or None, db [E] or None), fp64."""
+    x, code = _act(x)
+    N, d = x.shape
+    Wr = np.ascontiguousarray(w_router, dtype=np.float32)
+    E = Wr.shape[0]
+    dl = np.ascontiguousarray(dl, dtype=np.float64)
+    tokens = np.arange(N, dtype=np.int32) if tokens is None else \
+        np.ascontiguousarray(tokens, dtype=np.int32)
+    dxr = np.empty((tokens.size, d), np.float64)
+    dwr = np.empty((E, d), np.float64) if params else None
+    db = np.empty(E, np.float64) if params else None
+    _lib().oracle_router_grads(N, d, E, code, _p(x), _p(Wr), _p(dl), tokens.size, _p(tokens),
+                               _p(dxr), _p(dwr), _p(db))
+    return dxr, dwr, db
+
+
+def dispatch_backward(tokens, dout, dxperm, slot_of, dxs=None, dxr=None):
+    dout, code = _act(dout)
+    dxperm, c1 = _act(dxperm)
+    assert code == c1
+    N, d = dout.shape
+    slot_of = np.ascontiguousarray(slot_of, dtype=np.int32).reshape(-1)
+    k = slot_of.size // N
+    if dxs is not None:
+        dxs, c2 = _act(dxs)
+        assert c2 == code
+    dxr = None if dxr is None else np.ascontiguousarray(dxr, dtype=np.float32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    out = np.empty((tokens.size, d), np.float64)
+    _lib().oracle_dispatch_backward(tokens.size, _p(tokens), d, k, code, _p(dout), _p(dxs),
+                                    _p(dxr), _p(dxperm), _p(slot_of), _p(out))
     return out

@@ -16,6 +16,9 @@
 //   8. bias update        sign rule, fp32
 //   9. INT8 payload       per-row symmetric quantisation of the rows an all-to-all
 //                         sends, and the receiver's dequantisation and combine
+//  10. backward           gradients of the layer output with respect to the hidden
+//                         states, the expert and shared-expert weights and the router
+//                         weight and bias (the selection itself is piecewise constant)
 //
 // Sources ("the pages"):
 //   [UG] Ultralytics glossary "Expert Parallelism" (Chinese, German and Japanese
@@ -632,6 +635,287 @@ int oracle_combine_q8(int ntok, const int32_t* tokens, int d, int k, int act_dty
 // fp32 -> bf16 bits (round to nearest even), exposed for its own pin.
 int oracle_float_to_bf16(int64_t n, const float* in, uint16_t* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = float_to_bf16_rne(in[i]);
+  return 0;
+}
+
+// ---------------------------------------------------------------- 10. backward
+//
+// The layer of sections 1-7 for a fixed selection (the top-k choice, the capacity
+// drops and the group limit are piecewise constant in the inputs, so they pass no
+// gradient; the selection-only bias has none and is moved by the sign rule of
+// section 8 instead).  With dout = dL/dout:
+//   combine      dy_j = w_j * dout (kept j);  dw_j = dout . y_j (kept j), 0 if dropped
+//   residual     dout flows to x unchanged;  shared expert: its dy is dout itself
+//   expert FFN   g = Wg x, u = Wu x, h = silu(g) * u, y = Wd h:
+//                dh = Wd^T dy;  dg = dh * u * silu'(g);  du = dh * silu(g)
+//                dx = Wg^T dg + Wu^T du;  dWd += dy h^T;  dWg += dg x^T;  dWu += du x^T
+//                silu'(z) = s(z) (1 + z (1 - s(z))), s = the logistic function
+//   router       weights from logits l (section 2):
+//                softmax, normalised:   w_j = exp(l_j) / sum_sel exp  ->
+//                                       dl_j = w_j (dw_j - sum_i w_i dw_i), 0 off the selection
+//                softmax, unnormalised: w_j = p_j, p = softmax over all E ->
+//                                       dl_e = p_e (dw_e - sum_j w_j dw_j), dw_e = 0 off the selection
+//                sigmoid, normalised:   w_j = s_j / sum_sel s ->
+//                                       dl_j = s_j (1 - s_j) (dw_j - sum_i w_i dw_i) / sum_sel s
+//                sigmoid, unnormalised: dl_j = s_j (1 - s_j) dw_j
+//                (s_j = S(l_j), the fp32 function of section 2, as in the forward;
+//                its derivative is that of the logistic function)
+//                dx += Wr^T dl;  dWr += dl x^T;  db += dl
+//   dispatch     dx[t] = dout[t] + dx_shared[t] + dx_router[t] + sum_{j kept} dx_j
+// All in fp64.
+
+// Combine backward.  dout [N, d] act; yperm [*, d] act (the forward's expert rows);
+// slot_of [N*k]; w [N*k] fp64.  dy [*, d] fp64 written at the kept slots only;
+// dw [N*k] fp64 (0 for dropped choices).
+int oracle_combine_backward(int N, int d, int k, int act_dtype, const void* dout,
+                            const void* yperm, const int32_t* slot_of, const double* w,
+                            double* dy, double* dw) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < N; ++t) {
+    for (int j = 0; j < k; ++j) {
+      const int64_t a = static_cast<int64_t>(t) * k + j;
+      const int32_t s = slot_of[a];
+      if (s < 0) {
+        dw[a] = 0.0;
+        continue;
+      }
+      double dot = 0.0;
+      for (int c = 0; c < d; ++c) {
+        const double g = load_act(dout, act_dtype, static_cast<int64_t>(t) * d + c);
+        dot += g * load_act(yperm, act_dtype, static_cast<int64_t>(s) * d + c);
+        dy[static_cast<int64_t>(s) * d + c] = w[a] * g;
+      }
+      dw[a] = dot;
+    }
+  }
+  return 0;
+}
+
+namespace {
+inline double logistic(double z) { return 1.0 / (1.0 + std::exp(-z)); }
+
+// g, u of one row for the gate/up rows f (fp64).
+inline void gate_up_at(const double* x, int d, int F, int act_dtype, const void* wgu,
+                       int64_t wgu_off, int f, double* g, double* u) {
+  double a = 0.0, b = 0.0;
+  const int64_t rg = wgu_off + static_cast<int64_t>(f) * d;
+  const int64_t ru = wgu_off + static_cast<int64_t>(F + f) * d;
+  for (int i = 0; i < d; ++i) {
+    a += x[i] * load_act(wgu, act_dtype, rg + i);
+    b += x[i] * load_act(wgu, act_dtype, ru + i);
+  }
+  *g = a;
+  *u = b;
+}
+
+// dh_f = sum_o dy_o Wd[o][f]
+inline double dh_at(const double* dy, int d, int F, int act_dtype, const void* wd, int64_t wd_off,
+                    int f) {
+  double acc = 0.0;
+  for (int o = 0; o < d; ++o)
+    acc += dy[o] * load_act(wd, act_dtype, wd_off + static_cast<int64_t>(o) * F + f);
+  return acc;
+}
+}  // namespace
+
+// Expert FFN backward, input gradient of each row.  Row r belongs to expert
+// expert[r] (E = the shared expert); x rows and dy rows in act_dtype.
+// dx [n, d] fp64.
+int oracle_ffn_backward_rows(int n, int d, int E, int F, int Fs, int act_dtype, const void* xrows,
+                             const void* dyrows, const int32_t* expert, const void* w_gate_up,
+                             const void* w_down, const void* shared_gate_up,
+                             const void* shared_down, double* dx) {
+#pragma omp parallel
+  {
+    std::vector<double> xr(d), dyr(d), dg, du;
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < n; ++r) {
+      for (int c = 0; c < d; ++c) {
+        xr[c] = load_act(xrows, act_dtype, static_cast<int64_t>(r) * d + c);
+        dyr[c] = load_act(dyrows, act_dtype, static_cast<int64_t>(r) * d + c);
+      }
+      const int e = expert[r];
+      const bool sh = e >= E;
+      const int Fx = sh ? Fs : F;
+      const void* wgu = sh ? shared_gate_up : w_gate_up;
+      const void* wd = sh ? shared_down : w_down;
+      const int64_t gu_off = sh ? 0 : static_cast<int64_t>(e) * 2 * F * d;
+      const int64_t d_off = sh ? 0 : static_cast<int64_t>(e) * d * F;
+      dg.assign(Fx, 0.0);
+      du.assign(Fx, 0.0);
+      for (int f = 0; f < Fx; ++f) {
+        double g, u;
+        gate_up_at(xr.data(), d, Fx, act_dtype, wgu, gu_off, f, &g, &u);
+        const double dh = dh_at(dyr.data(), d, Fx, act_dtype, wd, d_off, f);
+        const double sg = logistic(g);
+        dg[f] = dh * u * sg * (1.0 + g * (1.0 - sg));
+        du[f] = dh * g * sg;
+      }
+      double* o = dx + static_cast<int64_t>(r) * d;
+      for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int f = 0; f < Fx; ++f) {
+          acc += dg[f] * load_act(wgu, act_dtype, gu_off + static_cast<int64_t>(f) * d + i);
+          acc += du[f] * load_act(wgu, act_dtype, gu_off + static_cast<int64_t>(Fx + f) * d + i);
+        }
+        o[i] = acc;
+      }
+    }
+  }
+  return 0;
+}
+
+// Weight gradients of one expert (or the shared expert) from its n rows, for the
+// listed hidden units f (nf of them; pass all 0..Fx-1 for the full gradients):
+//   dWd[:, f]   = sum_r dy_r h_r[f]        -> dwd_cols [nf, d]  (column f of dWd, as a row)
+//   dWg[f, :]   = sum_r dg_r[f] x_r        -> dwg_rows [nf, d]
+//   dWu[f, :]   = sum_r du_r[f] x_r        -> dwu_rows [nf, d]
+// wgu / wd point at this expert's [2Fx, d] and [d, Fx] weights.
+int oracle_ffn_wgrad(int n, int d, int Fx, int act_dtype, const void* xrows, const void* dyrows,
+                     const void* wgu, const void* wd, int nf, const int32_t* fs,
+                     double* dwd_cols, double* dwg_rows, double* dwu_rows) {
+#pragma omp parallel
+  {
+    std::vector<double> xr(d), dyr(d);
+#pragma omp for schedule(dynamic, 1)
+    for (int q = 0; q < nf; ++q) {
+      const int f = fs[q];
+      double* cd = dwd_cols + static_cast<int64_t>(q) * d;
+      double* rg = dwg_rows + static_cast<int64_t>(q) * d;
+      double* ru = dwu_rows + static_cast<int64_t>(q) * d;
+      for (int i = 0; i < d; ++i) cd[i] = rg[i] = ru[i] = 0.0;
+      for (int r = 0; r < n; ++r) {
+        for (int c = 0; c < d; ++c) {
+          xr[c] = load_act(xrows, act_dtype, static_cast<int64_t>(r) * d + c);
+          dyr[c] = load_act(dyrows, act_dtype, static_cast<int64_t>(r) * d + c);
+        }
+        double g, u;
+        gate_up_at(xr.data(), d, Fx, act_dtype, wgu, 0, f, &g, &u);
+        const double sg = logistic(g);
+        const double h = g * sg * u;
+        const double dh = dh_at(dyr.data(), d, Fx, act_dtype, wd, 0, f);
+        const double dgv = dh * u * sg * (1.0 + g * (1.0 - sg));
+        const double duv = dh * g * sg;
+        for (int i = 0; i < d; ++i) {
+          cd[i] += dyr[i] * h;
+          rg[i] += dgv * xr[i];
+          ru[i] += duv * xr[i];
+        }
+      }
+    }
+  }
+  return 0;
+}
+
+// Router backward, logits gradient.  logits [N, E] fp32 (the forward's), idx [N, k],
+// dw [N, k] fp64 (from the combine backward; 0 for dropped choices).  dl [N, E] fp64.
+int oracle_route_backward(int N, int E, int k, int score_fn, int normalize, const float* logits,
+                          const int32_t* idx, const double* dw, double* dl) {
+#pragma omp parallel
+  {
+    std::vector<double> w(k), sv(k);
+#pragma omp for schedule(static)
+    for (int t = 0; t < N; ++t) {
+      const float* l = logits + static_cast<int64_t>(t) * E;
+      const int32_t* id = idx + static_cast<int64_t>(t) * k;
+      const double* g = dw + static_cast<int64_t>(t) * k;
+      double* o = dl + static_cast<int64_t>(t) * E;
+      for (int e = 0; e < E; ++e) o[e] = 0.0;
+      if (score_fn == 1) {
+        double ssum = 0.0;
+        for (int j = 0; j < k; ++j) {
+          sv[j] = static_cast<double>(sigmoid_spec(l[id[j]]));
+          ssum += sv[j];
+        }
+        if (normalize) {
+          double wdw = 0.0;
+          for (int j = 0; j < k; ++j) wdw += sv[j] / ssum * g[j];
+          for (int j = 0; j < k; ++j)
+            o[id[j]] = sv[j] * (1.0 - sv[j]) * (g[j] - wdw) / ssum;
+        } else {
+          for (int j = 0; j < k; ++j) o[id[j]] = sv[j] * (1.0 - sv[j]) * g[j];
+        }
+      } else {
+        double m = -INFINITY;
+        for (int e = 0; e < E; ++e) m = std::max(m, static_cast<double>(l[e]));
+        if (normalize) {
+          double zs = 0.0;
+          for (int j = 0; j < k; ++j) zs += std::exp(static_cast<double>(l[id[j]]) - m);
+          double wdw = 0.0;
+          for (int j = 0; j < k; ++j) {
+            w[j] = std::exp(static_cast<double>(l[id[j]]) - m) / zs;
+            wdw += w[j] * g[j];
+          }
+          for (int j = 0; j < k; ++j) o[id[j]] = w[j] * (g[j] - wdw);
+        } else {
+          double z = 0.0;
+          for (int e = 0; e < E; ++e) z += std::exp(static_cast<double>(l[e]) - m);
+          double wdw = 0.0;
+          for (int j = 0; j < k; ++j) wdw += std::exp(static_cast<double>(l[id[j]]) - m) / z * g[j];
+          for (int e = 0; e < E; ++e) o[e] = -std::exp(static_cast<double>(l[e]) - m) / z * wdw;
+          for (int j = 0; j < k; ++j)
+            o[id[j]] += std::exp(static_cast<double>(l[id[j]]) - m) / z * g[j];
+        }
+      }
+    }
+  }
+  return 0;
+}
+
+// Router parameter and input gradients from dl [N, E] (fp64):
+//   dx_router [ntok, d] for the listed tokens: dl[t] . Wr  (Wr [E, d] fp32)
+//   dWr [E, d] = sum_t dl[t, e] x[t]  and db [E] = sum_t dl[t, e]   (all N tokens;
+//   dwr / db may be null to skip them)
+int oracle_router_grads(int N, int d, int E, int act_dtype, const void* x, const float* Wr,
+                        const double* dl, int ntok, const int32_t* tokens, double* dx_router,
+                        double* dwr, double* db) {
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < ntok; ++i) {
+    const int64_t t = tokens[i];
+    for (int c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int e = 0; e < E; ++e) acc += dl[t * E + e] * static_cast<double>(Wr[static_cast<int64_t>(e) * d + c]);
+      dx_router[static_cast<int64_t>(i) * d + c] = acc;
+    }
+  }
+  if (dwr) {
+#pragma omp parallel for schedule(static)
+    for (int e = 0; e < E; ++e) {
+      double* o = dwr + static_cast<int64_t>(e) * d;
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      double bsum = 0.0;
+      for (int t = 0; t < N; ++t) {
+        const double v = dl[static_cast<int64_t>(t) * E + e];
+        if (v == 0.0) continue;
+        bsum += v;
+        for (int c = 0; c < d; ++c) o[c] += v * load_act(x, act_dtype, static_cast<int64_t>(t) * d + c);
+      }
+      if (db) db[e] = bsum;
+    }
+  }
+  return 0;
+}
+
+// Dispatch backward for the listed tokens: dx[t] = dout[t] + dxs[t] + dxr[t] +
+// sum_{j kept} dxperm[slot_of[t, j]].  dout, dxs, dxperm act_dtype (dxs may be null);
+// dxr fp32 [N, d] or null.  out [ntok, d] fp64.
+int oracle_dispatch_backward(int ntok, const int32_t* tokens, int d, int k, int act_dtype,
+                             const void* dout, const void* dxs, const float* dxr,
+                             const void* dxperm, const int32_t* slot_of, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < ntok; ++i) {
+    const int64_t t = tokens[i];
+    for (int c = 0; c < d; ++c) {
+      double acc = load_act(dout, act_dtype, t * d + c);
+      if (dxs) acc += load_act(dxs, act_dtype, t * d + c);
+      if (dxr) acc += static_cast<double>(dxr[t * d + c]);
+      for (int j = 0; j < k; ++j) {
+        const int32_t s = slot_of[t * k + j];
+        if (s >= 0) acc += load_act(dxperm, act_dtype, static_cast<int64_t>(s) * d + c);
+      }
+      out[static_cast<int64_t>(i) * d + c] = acc;
+    }
+  }
   return 0;
 }
 
