@@ -395,6 +395,103 @@ moe_status moe_combine_q8(const moe_config* cfg, const int8_t* yperm_q, const fl
                                      static_cast<cudaStream_t>(stream)));
 }
 
+// ---------------------------------------------------------------- backward
+moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = 256 + round_up(ffn_backward_ws_bytes(c));
+  return MOE_OK;
+}
+
+moe_status moe_combine_backward(const moe_config* cfg, const void* dout, const void* yperm,
+                                const int32_t* slot_of, const float* topk_w, void* dyperm,
+                                float* dtopk_w, void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!dout || !yperm || !slot_of || !topk_w || !dyperm || !dtopk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(dout, 16) || !aligned(yperm, 16) || !aligned(dyperm, 16) || !aligned(slot_of, 4) ||
+      !aligned(topk_w, 4) || !aligned(dtopk_w, 4))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  return from_cuda(launch_combine_backward(c, dout, yperm, slot_of, topk_w, dyperm, dtopk_w,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xperm,
+                                   const int32_t* expert_start, const int32_t* kept_counts,
+                                   const void* w_gate_up, const void* w_down, const void* x,
+                                   const void* shared_gate_up, const void* shared_down,
+                                   const void* dyperm, const void* dout, void* dxperm,
+                                   void* dx_shared, void* dw_gate_up, void* dw_down,
+                                   void* dshared_gate_up, void* dshared_down, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (c.act != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  const void* req[] = {xperm, w_gate_up, w_down, dyperm, dxperm, dw_gate_up, dw_down};
+  for (const void* q : req)
+    if (!q || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+  if (!expert_start || !kept_counts || !aligned(expert_start, 4) || !aligned(kept_counts, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (c.Fs > 0) {
+    const void* sh[] = {x, shared_gate_up, shared_down, dout, dx_shared, dshared_gate_up,
+                        dshared_down};
+    for (const void* q : sh)
+      if (!q || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+  }
+  size_t need = 0;
+  if ((st = moe_backward_workspace_size(cfg, &need)) != MOE_OK) return st;
+  if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+  if ((st = check_device()) != MOE_OK) return st;
+  int* status = static_cast<int*>(workspace);
+  return from_cuda(launch_ffn_backward(c, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
+                                       shared_gate_up, shared_down, dyperm, dout, dxperm,
+                                       dx_shared, dw_gate_up, dw_down, dshared_gate_up,
+                                       dshared_down, static_cast<char*>(workspace) + 256, status,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route_backward(const moe_config* cfg, const void* x, const float* w_router,
+                              const float* logits, const int32_t* topk_idx, const float* dtopk_w,
+                              float* dlogits, float* dx_router, float* dw_router,
+                              float* db_router, void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!logits || !topk_idx || !dtopk_w || !dlogits) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(topk_idx, 4) || !aligned(dtopk_w, 4) || !aligned(dlogits, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (dx_router && (!w_router || !aligned(w_router, 16) || !aligned(dx_router, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if ((dw_router == nullptr) != (db_router == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (dw_router && (!x || !aligned(x, 16) || !aligned(dw_router, 4) || !aligned(db_router, 4)))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  return from_cuda(launch_route_backward(c, x, w_router, logits, topk_idx, dtopk_w, dlogits,
+                                         dx_router, dw_router, db_router,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_backward(const moe_config* cfg, const void* dxperm, const int32_t* slot_of,
+                                 const void* dout, const void* dx_shared, const float* dx_router,
+                                 void* dx, void* stream) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!dxperm || !slot_of || !dout || !dx) return MOE_ERR_INVALID_ARG;
+  if (!aligned(dxperm, 16) || !aligned(dout, 16) || !aligned(dx, 16) || !aligned(slot_of, 4) ||
+      (dx_shared && !aligned(dx_shared, 16)) || (dx_router && !aligned(dx_router, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  return from_cuda(launch_dispatch_backward(c, dxperm, slot_of, dout, dx_shared, dx_router, dx,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "MOE_OK: success";

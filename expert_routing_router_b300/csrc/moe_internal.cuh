@@ -132,5 +132,26 @@ cudaError_t launch_dequant_rows(const Cfg& c, const int8_t* q, const float* scal
 cudaError_t launch_combine_q8(const Cfg& c, const int8_t* yq, const float* yscale,
                               const int32_t* slot_of, const float* topk_w, const void* residual,
                               const void* yshared, void* out, cudaStream_t s);
+// backward (backward.cu, ffn_bwd_tc.cu)
+cudaError_t launch_combine_backward(const Cfg& c, const void* dout, const void* yperm,
+                                    const int32_t* slot_of, const float* topk_w, void* dyperm,
+                                    float* dtopk_w, cudaStream_t s);
+cudaError_t launch_route_backward(const Cfg& c, const void* x, const float* w_router,
+                                  const float* logits, const int32_t* topk_idx,
+                                  const float* dtopk_w, float* dlogits, float* dx_router,
+                                  float* dw_router, float* db_router, cudaStream_t s);
+cudaError_t launch_dispatch_backward(const Cfg& c, const void* dxperm, const int32_t* slot_of,
+                                     const void* dout, const void* dx_shared,
+                                     const float* dx_router, void* dx, cudaStream_t s);
+cudaError_t launch_zero_empty_experts(const Cfg& c, void* dw_gate_up, void* dw_down,
+                                      const int32_t* kept_counts, cudaStream_t s);
+size_t ffn_backward_ws_bytes(const Cfg& c);
+cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* expert_start,
+                                const int32_t* kept_counts, const void* w_gate_up,
+                                const void* w_down, const void* x, const void* shared_gate_up,
+                                const void* shared_down, const void* dyperm, const void* dout,
+                                void* dxperm, void* dx_shared, void* dw_gate_up, void* dw_down,
+                                void* dshared_gate_up, void* dshared_down, void* ws, int* status,
+                                cudaStream_t s);
 int num_sms();
 }  // namespace moe

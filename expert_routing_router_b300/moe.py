@@ -38,7 +38,8 @@ class MoeError(RuntimeError):
 EXPORTS = ("moe_send_rows", "moe_workspace_size", "moe_route", "moe_dispatch", "moe_dispatch_noalloc",
            "moe_expert_ffn", "moe_selftest_ffn_stall", "moe_combine", "moe_bias_update",
            "moe_dispatch_q8", "moe_quant_rows", "moe_dequant_rows", "moe_combine_q8",
-           "moe_status_string")
+           "moe_backward_workspace_size", "moe_combine_backward", "moe_expert_ffn_backward",
+           "moe_route_backward", "moe_dispatch_backward", "moe_status_string")
 
 
 def _load():
@@ -61,6 +62,11 @@ def _load():
     lib.moe_quant_rows.argtypes = [C] + [P] * 4 + [P]
     lib.moe_dequant_rows.argtypes = [C] + [P] * 4 + [P]
     lib.moe_combine_q8.argtypes = [C] + [P] * 7 + [P]
+    lib.moe_backward_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_combine_backward.argtypes = [C] + [P] * 6 + [P]
+    lib.moe_expert_ffn_backward.argtypes = [C] + [P] * 17 + [S, P]
+    lib.moe_route_backward.argtypes = [C] + [P] * 9 + [P]
+    lib.moe_dispatch_backward.argtypes = [C] + [P] * 6 + [P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for fn in EXPORTS[:-1]:
@@ -195,6 +201,90 @@ def moe_combine_q8(cfg, yperm_q, yscale, slot_of, topk_w, residual, yshared, out
     _check("moe_combine_q8", _lib.moe_combine_q8(
         ctypes.byref(cfg), _p(yperm_q), _p(yscale), _p(slot_of), _p(topk_w), _p(residual),
         _p(yshared), _p(out), _stream(stream)))
+
+
+# ------------------------------------------------------------------ backward
+
+def moe_backward_workspace_size(cfg):
+    n = ctypes.c_size_t(0)
+    _check("moe_backward_workspace_size",
+           _lib.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def moe_combine_backward(cfg, dout, yperm, slot_of, topk_w, dyperm, dtopk_w, stream=None):
+    _check("moe_combine_backward", _lib.moe_combine_backward(
+        ctypes.byref(cfg), _p(dout), _p(yperm), _p(slot_of), _p(topk_w), _p(dyperm),
+        _p(dtopk_w), _stream(stream)))
+
+
+def moe_expert_ffn_backward(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
+                            shared_gate_up, shared_down, dyperm, dout, dxperm, dx_shared,
+                            dw_gate_up, dw_down, dshared_gate_up, dshared_down, workspace,
+                            stream=None):
+    _check("moe_expert_ffn_backward", _lib.moe_expert_ffn_backward(
+        ctypes.byref(cfg), _p(xperm), _p(expert_start), _p(kept_counts), _p(w_gate_up),
+        _p(w_down), _p(x), _p(shared_gate_up), _p(shared_down), _p(dyperm), _p(dout),
+        _p(dxperm), _p(dx_shared), _p(dw_gate_up), _p(dw_down), _p(dshared_gate_up),
+        _p(dshared_down), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_route_backward(cfg, x, w_router, logits, topk_idx, dtopk_w, dlogits, dx_router,
+                       dw_router, db_router, stream=None):
+    _check("moe_route_backward", _lib.moe_route_backward(
+        ctypes.byref(cfg), _p(x), _p(w_router), _p(logits), _p(topk_idx), _p(dtopk_w),
+        _p(dlogits), _p(dx_router), _p(dw_router), _p(db_router), _stream(stream)))
+
+
+def moe_dispatch_backward(cfg, dxperm, slot_of, dout, dx_shared, dx_router, dx, stream=None):
+    _check("moe_dispatch_backward", _lib.moe_dispatch_backward(
+        ctypes.byref(cfg), _p(dxperm), _p(slot_of), _p(dout), _p(dx_shared), _p(dx_router),
+        _p(dx), _stream(stream)))
+
+
+class GradBuffers:
+    """Device buffers of one backward call (bf16 layers): gradients of the hidden
+    states, every weight and the router, plus the intermediates and the workspace."""
+
+    def __init__(self, w, device="cuda"):
+        N, d, E, k, F, Fs = w.tokens, w.hidden, w.num_experts, w.top_k, w.d_ff, w.shared_d_ff
+        dt = w.torch_dtype
+        f32 = dict(dtype=torch.float32, device=device)
+        self.cfg = config(w)
+        S = moe_send_rows(self.cfg)
+        self.dyperm = torch.empty(S, d, dtype=dt, device=device)
+        self.dtopk_w = torch.empty(N, k, **f32)
+        self.dxperm = torch.empty(S, d, dtype=dt, device=device)
+        self.dx_shared = torch.empty(N, d, dtype=dt, device=device) if Fs else None
+        self.dlogits = torch.empty(N, E, **f32)
+        self.dx_router = torch.empty(N, d, **f32)
+        self.dw_router = torch.empty(E, d, **f32)
+        self.db_router = torch.empty(E, **f32)
+        self.dx = torch.empty(N, d, dtype=dt, device=device)
+        self.dw_gate_up = torch.empty(E, 2 * F, d, dtype=dt, device=device)
+        self.dw_down = torch.empty(E, d, F, dtype=dt, device=device)
+        self.dshared_gate_up = torch.empty(2 * Fs, d, dtype=dt, device=device) if Fs else None
+        self.dshared_down = torch.empty(d, Fs, dtype=dt, device=device) if Fs else None
+        self.workspace = torch.empty(moe_backward_workspace_size(self.cfg), dtype=torch.uint8,
+                                     device=device)
+        self.workspace[:256].zero_()          # sticky device status word starts at 0
+
+
+def run_layer_backward(b, g, inp, dout, stream=None):
+    """Backward of the layer pass held in LayerBuffers b (selection fixed), from dout:
+    combine, expert FFN (recompute, dgrad, wgrad), router, dispatch.  Writes every
+    gradient into GradBuffers g and returns g.dx."""
+    c = b.cfg
+    moe_combine_backward(c, dout, b.yperm, b.slot_of, b.topk_w, g.dyperm, g.dtopk_w, stream)
+    moe_expert_ffn_backward(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
+                            inp["w_down"], inp["x"], inp["shared_gate_up"], inp["shared_down"],
+                            g.dyperm, dout, g.dxperm, g.dx_shared, g.dw_gate_up, g.dw_down,
+                            g.dshared_gate_up, g.dshared_down, g.workspace, stream)
+    moe_route_backward(c, inp["x"], inp["w_router"], b.logits, b.topk_idx, g.dtopk_w, g.dlogits,
+                       g.dx_router, g.dw_router, g.db_router, stream)
+    moe_dispatch_backward(c, g.dxperm, b.slot_of, dout, g.dx_shared, g.dx_router, g.dx, stream)
+    return g.dx
 
 
 class LayerBuffers:

@@ -297,6 +297,85 @@ MOE_API moe_status moe_combine_q8(const moe_config* cfg, const int8_t* yperm_q, 
                                   const int32_t* slot_of, const float* topk_w, const void* residual,
                                   const void* yshared, void* out, void* stream);
 
+/* ---- Backward pass ----------------------------------------------------------
+ * Gradients of the layer output (the forward calls above, bias update aside) for a
+ * FIXED selection: the top-k choice, capacity drops and group limit are piecewise
+ * constant in the inputs and pass no gradient; the selection-only bias gets none (the
+ * sign rule of moe_bias_update moves it).  With dout = dL/dout [N, hidden] act_dtype:
+ *   moe_combine_backward    dyperm, dtopk_w
+ *   moe_expert_ffn_backward dxperm, dx_shared, every expert weight gradient
+ *   moe_route_backward      dlogits, dx_router, dw_router, db_router
+ *   moe_dispatch_backward   dx = dout + dx_shared + dx_router + sum_j dxperm[slot_of]
+ * The forward's own buffers (logits, topk_idx, topk_w, slot_of, expert_start,
+ * kept_counts, xperm, yperm) are the inputs; they must be those of the same call. */
+
+/* Bytes of the workspace moe_expert_ffn_backward needs (status word + recomputed
+ * gate/up and h, and [dg | du], bf16). */
+MOE_API moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Combine backward.  Same page, step 4, differentiated: for each kept choice,
+ *   dyperm[slot_of[t,j]] = topk_w[t,j] * dout[t]          (act_dtype, one rounding)
+ *   dtopk_w[t,j]         = sum_i dout[t,i] * yperm[slot,i] (fp32; 0 for dropped j)
+ * dout [N, hidden], yperm / dyperm [S, hidden] act_dtype (16-byte aligned); slot_of
+ * [N*k] int32; topk_w, dtopk_w [N, k] fp32.  Rows of dyperm that hold no assignment
+ * are not written. */
+MOE_API moe_status moe_combine_backward(const moe_config* cfg, const void* dout, const void* yperm,
+                                        const int32_t* slot_of, const float* topk_w, void* dyperm,
+                                        float* dtopk_w, void* stream);
+
+/* Expert FFN backward (bf16 layers; fp32 returns MOE_ERR_UNSUPPORTED).  For each
+ * send-buffer row of expert e (and each token for the shared expert), with
+ * g = Wg x, u = Wu x, h = silu(g) * u, y = Wd h:
+ *   dh = Wd^T dy;  dg = dh * u * silu'(g);  du = dh * silu(g)
+ *   dx = Wg^T dg + Wu^T du;  dWd[e] += dy h^T;  dWg[e] += dg x^T;  dWu[e] += du x^T
+ * g, u and h are recomputed from xperm (tensor cores, fp32 accumulation; g, u, h and
+ * [dg | du] rounded to bf16).
+ *   xperm, expert_start, kept_counts, w_gate_up, w_down, x, shared_*  as moe_expert_ffn
+ *   dyperm [S, hidden]  from moe_combine_backward;  dout [N, hidden] (the shared
+ *                       expert's dy; NULL without a shared expert)
+ *   dxperm [S, hidden]  out: input gradient of the kept rows
+ *   dx_shared [N, hidden] out (NULL without a shared expert)
+ *   dw_gate_up [E, 2F, hidden], dw_down [E, hidden, F]  out (experts with no kept rows
+ *                       get zeros); dshared_gate_up [2Fs, hidden], dshared_down
+ *                       [hidden, Fs] out (NULL without a shared expert)
+ *   workspace           moe_backward_workspace_size bytes, 256-byte aligned; its
+ *                       first int32 is a sticky status word (caller zeroes it; nonzero
+ *                       if a kernel gave up a bounded wait). */
+MOE_API moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xperm,
+                                           const int32_t* expert_start, const int32_t* kept_counts,
+                                           const void* w_gate_up, const void* w_down, const void* x,
+                                           const void* shared_gate_up, const void* shared_down,
+                                           const void* dyperm, const void* dout, void* dxperm,
+                                           void* dx_shared, void* dw_gate_up, void* dw_down,
+                                           void* dshared_gate_up, void* dshared_down,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Router backward.  The combine weights as functions of the logits (moe_route):
+ *   softmax, renormalised:   dl_j = w_j (dw_j - sum_i w_i dw_i) on the selection, 0 off it
+ *   softmax, unnormalised:   dl_e = p_e (dw_e - sum_j w_j dw_j), dw_e = 0 off the selection
+ *   sigmoid, renormalised:   dl_j = s_j (1 - s_j) (dw_j - sum_i w_i dw_i) / sum_sel s
+ *   sigmoid, unnormalised:   dl_j = s_j (1 - s_j) dw_j
+ * (s = the selection sigmoid of moe_route, p = softmax over all experts), then
+ *   dx_router = dl . w_router  [N, hidden] fp32 (NULL to skip)
+ *   dw_router = dl^T x [E, hidden] fp32 and db_router = sum_t dl [E] fp32 (both or
+ *   neither NULL)
+ * logits [N, E] fp32 and topk_idx [N, k] from moe_route; dtopk_w from
+ * moe_combine_backward; dlogits [N, E] fp32 out. */
+MOE_API moe_status moe_route_backward(const moe_config* cfg, const void* x, const float* w_router,
+                                      const float* logits, const int32_t* topk_idx,
+                                      const float* dtopk_w, float* dlogits, float* dx_router,
+                                      float* dw_router, float* db_router, void* stream);
+
+/* Dispatch backward: the permute's transpose plus the residual, shared-expert and
+ * router paths, summed in fp32 and rounded once:
+ *   dx[t] = dout[t] + dx_shared[t] + dx_router[t] + sum_{j kept, ascending} dxperm[slot_of[t,j]]
+ * dxperm [S, hidden], dout / dx_shared (nullable) / dx [N, hidden] act_dtype;
+ * dx_router [N, hidden] fp32 (nullable). */
+MOE_API moe_status moe_dispatch_backward(const moe_config* cfg, const void* dxperm,
+                                         const int32_t* slot_of, const void* dout,
+                                         const void* dx_shared, const float* dx_router, void* dx,
+                                         void* stream);
+
 /* Static, NUL-terminated description of a status code (host pointer). */
 MOE_API const char* moe_status_string(moe_status status);
 

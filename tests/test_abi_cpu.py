@@ -140,3 +140,32 @@ def test_int8_payload_calls_validate_on_host(moe_lib):
                             P(FAKE), None) == moe_lib.MOE_ERR_INVALID_ARG
     assert L.moe_combine_q8(ctypes.byref(cfg), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE + 4),
                             None, P(FAKE), None) == moe_lib.MOE_ERR_INVALID_ARG
+
+
+def test_backward_calls_validate_on_host(moe_lib):
+    """Backward entry points: fp32 expert backward is unsupported, bad buffers are
+    rejected, and the workspace size covers the recomputed activations."""
+    P = ctypes.c_void_p
+    L = moe_lib.lib
+    c3 = moe_lib.config(W.DSV3_PREFILL)
+    need = moe_lib.moe_backward_workspace_size(c3)
+    # g, u, h and [dg | du] in bf16 for the send rows and the shared expert's tokens
+    assert need >= 2 * 5 * (8192 * 8 * 2048 + 8192 * 2048)
+    c0 = moe_lib.config(W.TINY_TOP2_F32)
+    n0 = moe_lib.moe_backward_workspace_size(c0)
+    args = [P(FAKE)] * 17
+    assert L.moe_expert_ffn_backward(ctypes.byref(c0), *args, P(FAKE), n0, None) == \
+        moe_lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_expert_ffn_backward(ctypes.byref(c3), *args, P(FAKE), need - 1, None) == \
+        moe_lib.MOE_ERR_WORKSPACE
+    bad = list(args)
+    bad[10] = None                      # the shared expert's dout is required
+    assert L.moe_expert_ffn_backward(ctypes.byref(c3), *bad, P(FAKE), need, None) == \
+        moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_backward(ctypes.byref(c3), P(FAKE + 8), *[P(FAKE)] * 5, None) == \
+        moe_lib.MOE_ERR_INVALID_ARG
+    # router: dW and db come as a pair
+    assert L.moe_route_backward(ctypes.byref(c3), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                P(FAKE), None, P(FAKE), None, None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch_backward(ctypes.byref(c3), P(FAKE), P(FAKE), None, None, None, P(FAKE),
+                                   None) == moe_lib.MOE_ERR_INVALID_ARG
