@@ -153,13 +153,13 @@ def test_backward_calls_validate_on_host(moe_lib):
     assert need >= 2 * 5 * (8192 * 8 * 2048 + 8192 * 2048)
     c0 = moe_lib.config(W.TINY_TOP2_F32)
     n0 = moe_lib.moe_backward_workspace_size(c0)
-    args = [P(FAKE)] * 17
+    args = [P(FAKE)] * 16               # every pointer before the workspace
     assert L.moe_expert_ffn_backward(ctypes.byref(c0), *args, P(FAKE), n0, None) == \
         moe_lib.MOE_ERR_UNSUPPORTED
     assert L.moe_expert_ffn_backward(ctypes.byref(c3), *args, P(FAKE), need - 1, None) == \
         moe_lib.MOE_ERR_WORKSPACE
     bad = list(args)
-    bad[10] = None                      # the shared expert's dout is required
+    bad[9] = None                       # the shared expert's dout is required
     assert L.moe_expert_ffn_backward(ctypes.byref(c3), *bad, P(FAKE), need, None) == \
         moe_lib.MOE_ERR_INVALID_ARG
     assert L.moe_combine_backward(ctypes.byref(c3), P(FAKE + 8), *[P(FAKE)] * 5, None) == \
