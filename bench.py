@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the timed backward pass (reported beside the forward metric)")
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                     help="override a workload field (e.g. num_experts=16), for small "
                          "profiling cases of the same kernels")
@@ -517,6 +519,11 @@ def run_native(a, w, rank, world, local):
         "clocks": clocks, "gpu_launches": launches_per_step(w) * a.steps,
         "device_status": status,
     }
+    if (not a.no_backward and w.act_dtype == "bf16" and getattr(w, "payload", "act") == "act"
+            and world == 1):
+        out["backward"] = time_backward(a, w, moe, b, inp, s, flush, pk)
+        fwd_bwd_ms = out["ms_per_step"] + out["backward"]["ms_per_step"]
+        out["backward"]["train_step_tokens_per_s"] = w.tokens / (fwd_bwd_ms * 1e-3)
     if getattr(w, "payload", "act") == "int8":
         out["cpu_baseline"] = None           # the oracle baseline times the bf16-payload layer
     elif rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -524,6 +531,83 @@ def run_native(a, w, rank, world, local):
         torch.cuda.empty_cache()
         out["cpu_baseline"] = cpu_baseline(w, oracle_inputs(inp))
     return out
+
+
+def time_backward(a, w, moe, b, inp, s, flush, pk):
+    """The layer's backward calls on the forward state held in b, timed like the
+    forward: one CUDA graph per call, events between the calls of each timed step,
+    L2 flushed between steps.  Reported beside the forward metric."""
+    dev = b.logits.device
+    s = torch.cuda.current_stream()      # the stream the calls below launch on
+    g = moe.GradBuffers(w, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(a.seed + 1000)
+    dout = torch.randn(w.tokens, w.hidden, generator=gen, device=dev).to(w.torch_dtype)
+    c = b.cfg
+    calls = [
+        ("combine_bwd", lambda: moe.moe_combine_backward(c, dout, b.yperm, b.slot_of, b.topk_w,
+                                                         g.dyperm, g.dtopk_w)),
+        ("expert_ffn_bwd", lambda: moe.moe_expert_ffn_backward(
+            c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"], inp["w_down"],
+            inp["x"], inp["shared_gate_up"], inp["shared_down"], g.dyperm, dout, g.dxperm,
+            g.dx_shared, g.dw_gate_up, g.dw_down, g.dshared_gate_up, g.dshared_down,
+            g.workspace)),
+        ("route_bwd", lambda: moe.moe_route_backward(c, inp["x"], inp["w_router"], b.logits,
+                                                     b.topk_idx, g.dtopk_w, g.dlogits,
+                                                     g.dx_router, g.dw_router, g.db_router)),
+        ("dispatch_bwd", lambda: moe.moe_dispatch_backward(c, g.dxperm, b.slot_of, dout,
+                                                           g.dx_shared, g.dx_router, g.dx)),
+    ]
+    for _ in range(a.warmup):
+        for _, f in calls:
+            f()
+    torch.cuda.synchronize()
+    runs = [f for _, f in calls]
+    if not a.no_graph:
+        runs = []
+        for _, f in calls:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                f()
+            runs.append(gr.replay)
+        for _ in range(a.warmup):
+            for r in runs:
+                r()
+        torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(runs) + 1)]
+           for _ in range(a.steps)]
+    clk = Clocks(dev.index)
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        flush.fill_(i & 0xff)
+        evs[i][0].record(s)
+        for j, r in enumerate(runs):
+            r()
+            evs[i][j + 1].record(s)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(runs))] for e in evs])
+    stage = {n: float(v) for (n, _), v in zip(calls, per.mean(axis=0))}
+    step_ms = float(per.sum(axis=1).mean())
+    status = int(g.workspace[:4].view(torch.int32).item())
+    nk = int(b.num_kept.item())
+    rows_f = w.d_ff * nk + w.shared_d_ff * (w.tokens if w.shared_d_ff else 0)
+    alg = 12.0 * w.hidden * rows_f      # dgrad (2 GEMMs) + wgrad (2 GEMMs)
+    exe = 16.0 * w.hidden * rows_f      # plus the recomputed gate/up GEMM
+    t = stage["expert_ffn_bwd"] * 1e-3
+    del g
+    return {"metric": "MoE-layer backward tokens/s", "value": w.tokens / (step_ms * 1e-3),
+            "unit": "tokens/s", "ms_per_step": step_ms,
+            "train_step_tokens_per_s": None,
+            "stage_ms": dict(stage, note="events between the calls of each timed step"),
+            "expert_ffn_bwd": {"bound": "tensor", "unit": "TFLOP/s",
+                               "achieved": alg / t / 1e12, "executed": exe / t / 1e12,
+                               "peak": pk["bf16"], "frac": alg / t / 1e12 / pk["bf16"],
+                               "frac_executed": exe / t / 1e12 / pk["bf16"],
+                               "algorithmic_flops": alg,
+                               "note": "achieved counts dgrad+wgrad (12 d F per row); executed "
+                                       "adds the recomputed gate/up GEMM (16 d F per row)"},
+            "clocks": clocks, "gpu_launches": 12 * a.steps, "device_status": status}
 
 
 # ------------------------------------------------------------------ reference arm

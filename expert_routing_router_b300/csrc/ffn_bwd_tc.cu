@@ -20,12 +20,19 @@
 // TMA boxes, one 128-byte row per K index, descriptors with a leading offset of one
 // box (8 KiB) between 64-element MN chunks and 1 KiB between 8-row K groups, and the
 // instruction descriptor's transpose bit for that operand.
-// W1/W2 sum over a segment's rows: the last K block of a segment is loaded past its
-// end (the next segment's rows, or send-buffer rows never written), so before that
-// block's MMAs the MMA warp zeroes those rows of both tiles in shared memory (whole
-// 128-byte rows, which the swizzle only permutes internally) and fences them for the
-// tensor core.  Experts with no
-// rows get no W tiles; their gradients are zeroed by a separate kernel.
+// W1/W2 sum over a segment's rows, so a segment's rows must end in zeros up to the
+// next 64-row block (otherwise the last K block would add the next segment's rows, or
+// send-buffer rows never written).  The routed rows therefore live in a padded copy:
+// expert e's rows start at pad_start[e] (a prefix sum of its row count rounded up to
+// 64), and the rows up to that boundary are zero.  pad_rows_kernel copies xperm and
+// dY into that layout once per call; R1 and D1 then produce g, u, h and [dg | du] in it
+// (their padding rows come out zero, being products of zero rows).  The shared expert's
+// rows end where its tensors end, and TMA fills the rest of a block with zeros.
+// Experts with no rows get no W tiles; their gradients are zeroed by a separate kernel.
+// The W kinds' K loops are short (one segment's rows), so their output write is the
+// critical path: each tile is staged in shared memory (128-byte swizzle) and written
+// with TMA tensor stores into [segments, M, N] maps that clip a segment's row tail;
+// the ring has 3 stages there to make room.
 // Every mbarrier wait is bounded (about 2 s) and reports through the status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -39,6 +46,7 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int OUT_BYTES = BM * BN * 2;  // W kinds: one bf16 output tile staged for TMA stores
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -55,6 +63,10 @@ struct Traits {
   static constexpr bool a_mn = KIND == W1 || KIND == W2;   // A loaded MN-major
   static constexpr bool b_mn = KIND != R1;                  // B loaded MN-major
   static constexpr bool k_rows = KIND == W1 || KIND == W2;  // reduction over segment rows
+  // W kinds: short K loops (a segment's rows) make the output write the critical path;
+  // the tile goes out through shared memory and TMA stores, which costs one ring stage
+  static constexpr bool tma_out = k_rows;
+  static constexpr int stages = tma_out ? 3 : STAGES;
   static constexpr uint32_t idesc =
       idesc_bf16_f32(BM, BN) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
 };
@@ -62,6 +74,7 @@ struct Traits {
 struct BwdParams {
   const int32_t* expert_start;
   const int32_t* kept_counts;
+  const int32_t* pad_start;  // [E + 1] padded row starts of the routed segments
   __nv_bfloat16* out0;  // routed output   R1 gu, D1 dgu, D2 dx, W1 dWd, W2 dWgu
   __nv_bfloat16* out1;  // shared output
   __nv_bfloat16* aux0;  // R1: h out (routed) / D1: gu in (routed)
@@ -71,16 +84,44 @@ struct BwdParams {
 };
 
 struct Ctl {
-  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, esync;
   uint32_t tmem_base;
   int abort;
   int tile_start[MAX_SEG + 1];
   int mtiles[MAX_SEG];
   int rows[MAX_SEG];
-  int row_base[MAX_SEG];
+  int row_base[MAX_SEG];  // first row in the (padded) operand layout
+  int out_base[MAX_SEG];  // first row of the segment in the send buffer (dX rows)
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
+template <int KIND>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Traits<KIND>::stages * STAGE_BYTES +
+         (Traits<KIND>::tma_out ? OUT_BYTES : 0) + sizeof(Ctl);
+}
+
+// TMA store of one 64-column x 128-row box of a [segments, M, N] tensor (rows past a
+// segment's M are clipped by the map), then commit it to this thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x,
+                                             int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(saddr(src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 
 __device__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl, int* err, int code) {
   if (mbar_try_wait(b, parity)) return true;
@@ -96,6 +137,16 @@ __device__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl, int* err, int 
       }
     }
   }
+}
+
+// Rendezvous of the 4 epilogue warps (an mbarrier, so that the wait is bounded like
+// every other): false if it expired or another role gave up.
+__device__ bool epi_sync(Ctl* ctl, uint32_t* phase, int* err) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->esync);
+  const bool ok = mbar_wait(&ctl->esync, *phase, ctl, err, 6);
+  *phase ^= 1;
+  return __all_sync(0xffffffffu, ok);
 }
 
 // MN-major 128-byte-swizzle descriptor: start >> 4, leading offset = one 64-element
@@ -124,7 +175,7 @@ template <int KIND>
 __device__ __forceinline__ int n_step() { return KIND == R1 ? BN / 2 : BN; }
 
 struct Tile {
-  int seg, m0, n0, M, N, K, row_base;
+  int seg, m0, n0, M, N, K, row_base, out_base;
   bool routed;
 };
 
@@ -144,6 +195,7 @@ __device__ __forceinline__ Tile decode(const Ctl* ctl, int nseg, int t, const Bw
   tl.m0 = (local % mt) * BM;
   tl.n0 = (local / mt) * n_step<KIND>();
   tl.row_base = ctl->row_base[lo];
+  tl.out_base = ctl->out_base[lo];
   return tl;
 }
 
@@ -152,17 +204,20 @@ template <int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
 ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+               const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                BwdParams p) {
   using Tr = Traits<KIND>;
+  constexpr int NST = Tr::stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)STAGES * STAGE_BYTES);
+  uint8_t* stage_out = smem + (size_t)NST * STAGE_BYTES;  // W kinds only
+  Ctl* ctl = reinterpret_cast<Ctl*>(stage_out + (Tr::tma_out ? OUT_BYTES : 0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nseg = p.E + (p.n_shared > 0 ? 1 : 0);
 
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], 1);
     }
@@ -171,6 +226,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       mbar_init(&ctl->tempty[a], 4);
     }
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->esync, 4);  // one arrival per epilogue warp
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -188,7 +244,8 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         const int mt = (M + BM - 1) / BM;
         ctl->mtiles[s] = mt > 0 ? mt : 1;
         ctl->rows[s] = cnt;
-        ctl->row_base[s] = routed ? p.expert_start[s] : 0;
+        ctl->row_base[s] = routed ? p.pad_start[s] : 0;
+        ctl->out_base[s] = routed ? p.expert_start[s] : 0;
         // a segment with no rows has nothing to compute (W kinds: its gradient is zeroed
         // elsewhere)
         v = (cnt > 0) ? mt * ((N + n_step<KIND>() - 1) / n_step<KIND>()) : 0;
@@ -252,7 +309,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1;
           }
@@ -260,7 +317,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       }
       if (!ok) {  // let this CTA's copies land before the CTA goes away
         const uint64_t t0 = now_ns();
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < NST; ++s)
           if (armed >> s & 1u)
             while (!mbar_try_wait(&ctl->full[s], armed_parity >> s & 1u) &&
                    now_ns() - t0 < WAIT_NS) {
@@ -292,30 +349,6 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           break;
         }
         uint8_t* sa = smem + (size_t)stage * STAGE_BYTES;
-        if (Tr::k_rows && tl.K - k0 < BK) {
-          // rows past the segment's end: zero them.  Every lane observes the copy's
-          // completion itself before writing over it.
-          if (!mbar_wait(&ctl->full[stage], phase, ctl, p.err, 5)) {
-            ok = false;
-          }
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          // Both operands: the rows past the last kept row of the send buffer may never
-          // have been written, and 0 times a NaN bit pattern is NaN.  A and B are six
-          // consecutive 64-row boxes (2 of A, 4 of B).
-          const int valid = tl.K - k0;
-          const int nz = BK - valid;
-          for (int i = lane; i < 6 * nz * 8; i += 32) {
-            const int box = i / (nz * 8), rem = i % (nz * 8);
-            const int row = valid + rem / 8, chunk = rem % 8;
-            *reinterpret_cast<uint4*>(sa + box * BOX_BYTES + row * 128 + chunk * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-        }
         if (lane == 0) {
           tc_fence_after();
           const uint32_t a0 = saddr(sa);
@@ -330,7 +363,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           tc_commit(&ctl->empty[stage]);
         }
         __syncwarp();
-        if (++stage == STAGES) {
+        if (++stage == NST) {
           stage = 0;
           phase ^= 1;
         }
@@ -353,14 +386,17 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
     int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0, esync_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode<KIND>(ctl, nseg, t, p);
       const int Fx = tl.routed ? p.F : p.Fs;
       if (!mbar_wait(&ctl->tfull[acc], acc_phase, ctl, p.err, 4)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      const bool valid = tl.m0 + r < tl.M;
+      // R1 / D1 also store a routed segment's padding rows (zeros, from zero inputs),
+      // so that W1 / W2 read zeros there
+      const int m_store = ((KIND == R1 || KIND == D1) && tl.routed) ? ((tl.M + 63) & ~63) : tl.M;
+      const bool valid = tl.m0 + r < m_store;
       __nv_bfloat16* out = tl.routed ? p.out0 : p.out1;
       if (KIND == R1) {
         // g in columns [0,128), u in [128,256): gu row (g at f, u at Fx + f) and h
@@ -439,11 +475,60 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             }
           }
         }
+      } else if (Tr::tma_out) {
+        // [M, N] tile of dW -> shared memory (four 64-column boxes, 128-byte swizzle:
+        // 16-byte chunk j of row r at r*128 + (j ^ (r & 7))*16) -> TMA stores.  The
+        // previous tile's stores must have read the buffer first.
+        if (threadIdx.x == 64) bulk_wait_read();
+        if (!epi_sync(ctl, &esync_phase, p.err)) break;
+        // four 32-column TMEM loads in flight per wait (the K loops are short, so the
+        // load latency is not hidden behind the next tile's MMAs)
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 128) {
+          uint32_t y[4][32];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tb + c0 + 32 * q4, y[q4]);
+          tmem_ld_wait(y[0]);
+#pragma unroll
+          for (int q4 = 1; q4 < 4; ++q4) tmem_regs_ready(y[q4]);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16(__uint_as_float(y[q4][2 * i]), __uint_as_float(y[q4][2 * i + 1]));
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int col = c0 + 32 * q4 + v * 8;
+              const int box = col >> 6, chunk = (col & 63) >> 3;
+              *reinterpret_cast<uint4*>(stage_out + box * (BM * 128) + r * 128 +
+                                        ((chunk ^ (r & 7)) << 4)) =
+                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+          }
+        }
+        // the accumulator can go back to the MMA warp before the stores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (!epi_sync(ctl, &esync_phase, p.err)) break;
+        if (threadIdx.x == 64) {
+          const CUtensorMap* mo = tl.routed ? &tmO0 : &tmO1;
+          const int z = tl.routed ? tl.seg : 0;
+          for (int b = 0; b < BN / 64; ++b)
+            if (tl.n0 + 64 * b < tl.N)
+              tma_store_3d(mo, stage_out + b * (BM * 128), tl.n0 + 64 * b, tl.m0, z);
+          bulk_commit();
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+        continue;
       } else {
         // plain bf16 store of the [M, N] result
         __nv_bfloat16* orow;
         if (KIND == D2) {
-          orow = out + (int64_t)(tl.row_base + tl.m0 + r) * tl.N;
+          orow = out + (int64_t)(tl.out_base + tl.m0 + r) * tl.N;
         } else {
           const int64_t seg_off = tl.routed ? (int64_t)tl.seg * tl.M * tl.N : 0;
           orow = out + seg_off + (int64_t)(tl.m0 + r) * tl.N;
@@ -474,6 +559,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (Tr::tma_out && threadIdx.x == 64) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -482,6 +568,47 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- padded layout
+// pad_start[e] = sum_{e' < e} ceil64(kept[e']), pad_start[E] = the total.  One CTA.
+__global__ void pad_plan_kernel(const int32_t* __restrict__ kept, int32_t* __restrict__ pad_start,
+                                int E) {
+  __shared__ int s[kMaxExperts + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s[e] = (kept[e] + 63) & ~63;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      pad_start[e] = acc;
+      acc += s[e];
+    }
+    pad_start[E] = acc;
+  }
+}
+
+// Rows of expert e (blockIdx.y): dst[pad_start[e] + r] = src[expert_start[e] + r] for
+// r < kept[e], zero up to the 64-row boundary; for both xperm and dY.
+__global__ void pad_rows_kernel(const uint4* __restrict__ x, const uint4* __restrict__ dy,
+                                uint4* __restrict__ xpad, uint4* __restrict__ dypad,
+                                const int32_t* __restrict__ expert_start,
+                                const int32_t* __restrict__ kept,
+                                const int32_t* __restrict__ pad_start, int vec) {
+  const int e = blockIdx.y;
+  const int n = kept[e], npad = (n + 63) & ~63;
+  const int64_t src0 = expert_start[e], dst0 = pad_start[e];
+  for (int r = blockIdx.x; r < npad; r += gridDim.x) {
+    const int64_t so = (src0 + r) * vec, d = (dst0 + r) * vec;
+    for (int v = threadIdx.x; v < vec; v += blockDim.x) {
+      uint4 a = make_uint4(0, 0, 0, 0), b = a;
+      if (r < n) {
+        a = x[so + v];
+        b = dy[so + v];
+      }
+      xpad[d + v] = a;
+      dypad[d + v] = b;
+    }
   }
 }
 
@@ -515,27 +642,50 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over [segs, rows, cols] (row-major), box 64 columns x 128 rows x 1,
+// 128-byte swizzle: the destination of the W kinds' tile stores.
+bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                  uint64_t segs) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cols, rows, segs};
+  const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  const cuuint32_t box[3] = {64, BM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int KIND>
 cudaError_t run(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                const CUtensorMap& b1, const BwdParams& p, cudaStream_t s) {
+                const CUtensorMap& b1, const CUtensorMap& o0, const CUtensorMap& o1,
+                const BwdParams& p, cudaStream_t s) {
   auto k = ffn_bwd_kernel<KIND>;
+  constexpr size_t bytes = smem_bytes<KIND>();
+  static_assert(bytes <= 232448, "shared memory per CTA");
   static bool attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
   if (!attr_set[dev & 63]) {
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     attr_set[dev & 63] = true;
   }
-  k<<<num_sms(), THREADS, SMEM_BYTES, s>>>(a0, a1, b0, b1, p);
+  k<<<num_sms(), THREADS, bytes, s>>>(a0, a1, b0, b1, o0, o1, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// Rows of the padded routed layout: every segment rounded up to 64 rows.
+static uint64_t padded_rows(const Cfg& c) { return (uint64_t)c.send_rows + 64ull * c.E; }
+
 size_t ffn_backward_ws_bytes(const Cfg& c) {
-  // gu [S, 2F] + [N, 2Fs], h [S, F] + [N, Fs], dgu [S, 2F] + [N, 2Fs], bf16
-  const size_t rows = (size_t)c.send_rows, n = (size_t)c.N;
-  return 2 * (rows * 5 * c.F + n * 5 * c.Fs);
+  // pad_start [E+1] int32 (256 B aligned); bf16: xpad, dypad [P, d]; gu [P, 2F] +
+  // [N, 2Fs]; h [P, F] + [N, Fs]; dgu [P, 2F] + [N, 2Fs]
+  const size_t P = padded_rows(c), n = (size_t)c.N;
+  const size_t table = ((size_t)(c.E + 1) * 4 + 255) & ~size_t(255);
+  return table + 2 * (P * (2 * (size_t)c.d + 5 * (size_t)c.F) + n * 5 * (size_t)c.Fs);
 }
 
 cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* expert_start,
@@ -547,36 +697,51 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
                                 cudaStream_t s) {
   using bf = __nv_bfloat16;
   const bool sh = c.Fs > 0;
-  const uint64_t S = (uint64_t)c.send_rows, N = (uint64_t)c.N, d = (uint64_t)c.d;
+  const uint64_t N = (uint64_t)c.N, d = (uint64_t)c.d;
   const uint64_t F = (uint64_t)c.F, Fs = (uint64_t)c.Fs, E = (uint64_t)c.E;
-  bf* gu = static_cast<bf*>(ws);
+  const uint64_t S = padded_rows(c);  // rows of the padded routed layout
+  int32_t* pad_start = static_cast<int32_t*>(ws);
+  bf* xpad = reinterpret_cast<bf*>(static_cast<char*>(ws) +
+                                   (((size_t)(c.E + 1) * 4 + 255) & ~size_t(255)));
+  bf* dypad = xpad + S * d;
+  bf* gu = dypad + S * d;
   bf* gu_s = gu + S * 2 * F;
   bf* h = gu_s + N * 2 * Fs;
   bf* h_s = h + S * F;
   bf* dgu = h_s + N * Fs;
   bf* dgu_s = dgu + S * 2 * F;
-  BwdParams p{expert_start, kept_counts, nullptr, nullptr, nullptr, nullptr, status,
-              c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
-  CUtensorMap a0, a1, b0, b1;
   cudaError_t e;
-  // R1: A = xperm / x (K-major over d); B = W_gu rows (K-major)
-  if (!make_map(&a0, xperm, d, S, 64, BM) || !make_map(&b0, w_gate_up, d, E * 2 * F, 64, BN / 2))
+  pad_plan_kernel<<<1, 256, 0, s>>>(kept_counts, pad_start, c.E);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    const dim3 grid(16, c.E);
+    pad_rows_kernel<<<grid, 256, 0, s>>>(
+        static_cast<const uint4*>(xperm), static_cast<const uint4*>(dyperm),
+        reinterpret_cast<uint4*>(xpad), reinterpret_cast<uint4*>(dypad), expert_start,
+        kept_counts, pad_start, (int)(d * 2 / 16));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  BwdParams p{expert_start, kept_counts, pad_start, nullptr, nullptr, nullptr, nullptr, status,
+              c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
+  CUtensorMap a0, a1, b0, b1, o0, o1;
+  // R1: A = padded xperm / x (K-major over d); B = W_gu rows (K-major)
+  if (!make_map(&a0, xpad, d, S, 64, BM) || !make_map(&b0, w_gate_up, d, E * 2 * F, 64, BN / 2))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
   if (sh && (!make_map(&a1, x, d, N, 64, BM) || !make_map(&b1, shared_gate_up, d, 2 * Fs, 64, BN / 2)))
     return cudaErrorInvalidValue;
   p.out0 = gu; p.out1 = gu_s; p.aux0 = h; p.aux1 = h_s;
-  if ((e = run<R1>(a0, a1, b0, b1, p, s)) != cudaSuccess) return e;
-  // D1: A = dY (K-major over d); B = W_down as [d rows, F columns], MN-major
-  if (!make_map(&a0, dyperm, d, S, 64, BM) || !make_map(&b0, w_down, F, E * d, 64, 64))
+  if ((e = run<R1>(a0, a1, b0, b1, a0, a0, p, s)) != cudaSuccess) return e;
+  // D1: A = padded dY (K-major over d); B = W_down as [d rows, F columns], MN-major
+  if (!make_map(&a0, dypad, d, S, 64, BM) || !make_map(&b0, w_down, F, E * d, 64, 64))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
   if (sh && (!make_map(&a1, dout, d, N, 64, BM) || !make_map(&b1, shared_down, Fs, d, 64, 64)))
     return cudaErrorInvalidValue;
   p.out0 = dgu; p.out1 = dgu_s; p.aux0 = gu; p.aux1 = gu_s;
-  if ((e = run<D1>(a0, a1, b0, b1, p, s)) != cudaSuccess) return e;
+  if ((e = run<D1>(a0, a1, b0, b1, a0, a0, p, s)) != cudaSuccess) return e;
   // D2: A = [dG | dU] (K-major over 2F); B = W_gu as [2F rows, d columns], MN-major
   if (!make_map(&a0, dgu, 2 * F, S, 64, BM) || !make_map(&b0, w_gate_up, d, E * 2 * F, 64, 64))
     return cudaErrorInvalidValue;
@@ -586,25 +751,33 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
     return cudaErrorInvalidValue;
   p.out0 = static_cast<bf*>(dxperm); p.out1 = static_cast<bf*>(dx_shared);
   p.aux0 = p.aux1 = nullptr;
-  if ((e = run<D2>(a0, a1, b0, b1, p, s)) != cudaSuccess) return e;
+  if ((e = run<D2>(a0, a1, b0, b1, a0, a0, p, s)) != cudaSuccess) return e;
   // W1: dWd[e] = dY_e^T H_e: A = dY MN-major ([rows, d]), B = H MN-major ([rows, F])
-  if (!make_map(&a0, dyperm, d, S, 64, 64) || !make_map(&b0, h, F, S, 64, 64))
+  if (!make_map(&a0, dypad, d, S, 64, 64) || !make_map(&b0, h, F, S, 64, 64))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
   if (sh && (!make_map(&a1, dout, d, N, 64, 64) || !make_map(&b1, h_s, Fs, N, 64, 64)))
     return cudaErrorInvalidValue;
+  // dWd [E, d, F] and the shared [d, Fs], written by TMA stores
+  if (!make_out_map(&o0, dw_down, F, d, E)) return cudaErrorInvalidValue;
+  o1 = o0;
+  if (sh && !make_out_map(&o1, dshared_down, Fs, d, 1)) return cudaErrorInvalidValue;
   p.out0 = static_cast<bf*>(dw_down); p.out1 = static_cast<bf*>(dshared_down);
-  if ((e = run<W1>(a0, a1, b0, b1, p, s)) != cudaSuccess) return e;
+  if ((e = run<W1>(a0, a1, b0, b1, o0, o1, p, s)) != cudaSuccess) return e;
   // W2: dW_gu[e] = [dG | dU]_e^T X_e: A = dGU MN-major ([rows, 2F]), B = X MN-major
-  if (!make_map(&a0, dgu, 2 * F, S, 64, 64) || !make_map(&b0, xperm, d, S, 64, 64))
+  if (!make_map(&a0, dgu, 2 * F, S, 64, 64) || !make_map(&b0, xpad, d, S, 64, 64))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
   if (sh && (!make_map(&a1, dgu_s, 2 * Fs, N, 64, 64) || !make_map(&b1, x, d, N, 64, 64)))
     return cudaErrorInvalidValue;
+  // dW_gu [E, 2F, d] and the shared [2Fs, d]
+  if (!make_out_map(&o0, dw_gate_up, d, 2 * F, E)) return cudaErrorInvalidValue;
+  o1 = o0;
+  if (sh && !make_out_map(&o1, dshared_gate_up, d, 2 * Fs, 1)) return cudaErrorInvalidValue;
   p.out0 = static_cast<bf*>(dw_gate_up); p.out1 = static_cast<bf*>(dshared_gate_up);
-  if ((e = run<W2>(a0, a1, b0, b1, p, s)) != cudaSuccess) return e;
+  if ((e = run<W2>(a0, a1, b0, b1, o0, o1, p, s)) != cudaSuccess) return e;
   return launch_zero_empty_experts(c, dw_gate_up, dw_down, kept_counts, s);
 }
 
