@@ -17,7 +17,8 @@
 //   router_dx_kernel         one CTA per token: dx_router[t] = sum_e dl[t,e] Wr[e]
 //                            (experts with dl = 0 skipped: k of E for renormalised or
 //                            sigmoid routing)
-//   router_dw_kernel         dWr and db: 64-expert x 64-column tiles over all tokens
+//   router_dw_kernel         dWr and db: 8-expert x 256-column slices over all tokens,
+//                            skipping the tokens whose gradient is zero there
 //   dispatch_bwd_kernel      one CTA per token: the gather-sum above
 //   zero_rows_kernel         zero the weight gradients of experts that received no rows
 #include "moe_internal.cuh"
@@ -88,19 +89,21 @@ combine_bwd_kernel(const T* __restrict__ dout, const T* __restrict__ yperm,
     }
     const T* grow = dout + (int64_t)t * d;
     for (int u = threadIdx.x; u < units; u += TB) {
-      float g[8], y[8], o[8];
+      // every load of this vector position first (k expert rows and dout), then math
+      float g[8], y[kMaxTopK][8], o[8];
       V8<T>::load(grow, u, g);
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (slots[j] >= 0) V8<T>::load(yperm + (int64_t)slots[j] * d, u, y[j]);
 #pragma unroll
       for (int j = 0; j < kMaxTopK; ++j) {
         if (slots[j] < 0) continue;
-        const int64_t s = slots[j];
-        V8<T>::load(yperm + s * d, u, y);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          dot[j] = fmaf(g[i], y[i], dot[j]);
+          dot[j] = fmaf(g[i], y[j][i], dot[j]);
           o[i] = w[j] * g[i];
         }
-        V8<T>::store(dyperm + s * d, u, o);
+        V8<T>::store(dyperm + (int64_t)slots[j] * d, u, o);
       }
     }
     // block sums of the k dot products, fixed order
@@ -211,25 +214,44 @@ route_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ t
   }
 }
 
-// dx_router[t, :] = sum_e dl[t, e] Wr[e, :], e ascending, experts with dl = 0 skipped.
+// dx_router[t, :] = sum_e dl[t, e] Wr[e, :], e ascending over the experts with dl != 0
+// (k of E for renormalised or sigmoid routing): warp 0 compacts the row's nonzero
+// (e, dl) pairs into shared memory in ascending order, then every thread sums its
+// float4 columns over that list.
 __global__ void __launch_bounds__(TB)
 router_dx_kernel(const float* __restrict__ dl, const float* __restrict__ Wr,
                  float* __restrict__ dx_router, int N, int E, int d) {
-  __shared__ float row[kMaxExperts];
+  __shared__ int ids[kMaxExperts];
+  __shared__ float vals[kMaxExperts];
+  __shared__ int count;
   const int v4 = d / 4;
   for (int t = blockIdx.x; t < N; t += gridDim.x) {
-    for (int e = threadIdx.x; e < E; e += TB) row[e] = dl[(int64_t)t * E + e];
+    if (threadIdx.x < 32) {
+      int n = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + threadIdx.x;
+        const float v = e < E ? dl[(int64_t)t * E + e] : 0.0f;
+        const unsigned nz = __ballot_sync(0xffffffffu, v != 0.0f);
+        if (v != 0.0f) {
+          const int pos = n + __popc(nz & ((1u << threadIdx.x) - 1u));
+          ids[pos] = e;
+          vals[pos] = v;
+        }
+        n += __popc(nz);
+      }
+      if (threadIdx.x == 0) count = n;
+    }
     __syncthreads();
+    const int n = count;
     for (int c = threadIdx.x; c < v4; c += TB) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int e = 0; e < E; ++e) {
-        const float s = row[e];
-        if (s == 0.0f) continue;  // uniform over the CTA
-        const float4 w = reinterpret_cast<const float4*>(Wr + (int64_t)e * d)[c];
-        acc.x = fmaf(s, w.x, acc.x);
-        acc.y = fmaf(s, w.y, acc.y);
-        acc.z = fmaf(s, w.z, acc.z);
-        acc.w = fmaf(s, w.w, acc.w);
+      for (int i = 0; i < n; ++i) {
+        const float sv = vals[i];
+        const float4 w = reinterpret_cast<const float4*>(Wr + (int64_t)ids[i] * d)[c];
+        acc.x = fmaf(sv, w.x, acc.x);
+        acc.y = fmaf(sv, w.y, acc.y);
+        acc.z = fmaf(sv, w.z, acc.z);
+        acc.w = fmaf(sv, w.w, acc.w);
       }
       reinterpret_cast<float4*>(dx_router + (int64_t)t * d)[c] = acc;
     }
@@ -237,53 +259,60 @@ router_dx_kernel(const float* __restrict__ dl, const float* __restrict__ Wr,
   }
 }
 
-// dWr [E, d] = sum_t dl[t, e] x[t, :] and db [E] = sum_t dl[t, e]: one CTA per
-// (64 experts x 64 columns) tile, tokens in chunks of 32 staged in shared memory;
-// each thread owns a 4 x 4 block of the tile.  fp32, tokens in ascending order.
-constexpr int RW_T = 32;
+// dWr [E, d] = sum_t dl[t, e] x[t, :] and db [E] = sum_t dl[t, e], tokens ascending.
+// One CTA per (8 experts x 256 columns): it scans the 8-expert slice of dl for all
+// tokens in chunks of 64 (staged in shared memory) and touches x only for the tokens
+// with a nonzero gradient there (about k/E of them per expert for renormalised or
+// sigmoid routing); each thread owns one column and 8 accumulators.
+constexpr int DW_E = 8, DW_T = 64;
 template <typename T>
 __global__ void __launch_bounds__(TB)
 router_dw_kernel(const float* __restrict__ dl, const T* __restrict__ x, float* __restrict__ dwr,
                  float* __restrict__ db, int N, int E, int d) {
-  __shared__ float sl[RW_T][64];
-  __shared__ float sx[RW_T][64];
-  const int e0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
-  const int te = (threadIdx.x / 16) * 4, tc = (threadIdx.x % 16) * 4;
-  float acc[4][4] = {};
-  float bsum[4] = {};
-  for (int t0 = 0; t0 < N; t0 += RW_T) {
-    for (int i = threadIdx.x; i < RW_T * 64; i += TB) {
-      const int r = i / 64, c = i % 64;
+  __shared__ float sl[DW_T][DW_E];
+  __shared__ int list[DW_T];
+  __shared__ int nlist;
+  const int e0 = blockIdx.y * DW_E;
+  const int c = blockIdx.x * TB + threadIdx.x;
+  float acc[DW_E] = {}, bsum[DW_E] = {};
+  for (int t0 = 0; t0 < N; t0 += DW_T) {
+    for (int i = threadIdx.x; i < DW_T * DW_E; i += TB) {
+      const int r = i / DW_E, e = i % DW_E;
       const int t = t0 + r;
-      sl[r][c] = (t < N && e0 + c < E) ? dl[(int64_t)t * E + e0 + c] : 0.0f;
-      sx[r][c] = (t < N && c0 + c < d) ? to_f32(x[(int64_t)t * d + c0 + c]) : 0.0f;
+      sl[r][e] = (t < N && e0 + e < E) ? dl[(int64_t)t * E + e0 + e] : 0.0f;
     }
     __syncthreads();
-#pragma unroll 4
-    for (int r = 0; r < RW_T; ++r) {
-      float a[4], b[4];
+    if (threadIdx.x < 32) {  // tokens of this chunk with any nonzero gradient, ascending
+      int n = 0;
+      for (int r0 = 0; r0 < DW_T; r0 += 32) {
+        const int r = r0 + threadIdx.x;
+        bool any = false;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = sl[r][te + i];
-        b[i] = sx[r][tc + i];
+        for (int e = 0; e < DW_E; ++e) any |= sl[r][e] != 0.0f;
+        const unsigned m = __ballot_sync(0xffffffffu, any);
+        if (any) list[n + __popc(m & ((1u << threadIdx.x) - 1u))] = r;
+        n += __popc(m);
       }
+      if (threadIdx.x == 0) nlist = n;
+    }
+    __syncthreads();
+    const int n = nlist;
+    for (int i = 0; i < n; ++i) {
+      const int r = list[i];
+      const float xv = c < d ? to_f32(x[(int64_t)(t0 + r) * d + c]) : 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        bsum[i] += a[i];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      for (int e = 0; e < DW_E; ++e) {
+        acc[e] = fmaf(sl[r][e], xv, acc[e]);
+        bsum[e] += sl[r][e];
       }
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = e0 + te + i;
-    if (e >= E) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (c0 + tc + j < d) dwr[(int64_t)e * d + c0 + tc + j] = acc[i][j];
-    if (blockIdx.x == 0 && tc == 0) db[e] = bsum[i];
+  for (int e = 0; e < DW_E; ++e) {
+    if (e0 + e >= E) break;
+    if (c < d) dwr[(int64_t)(e0 + e) * d + c] = acc[e];
+    if (blockIdx.x == 0 && threadIdx.x == 0) db[e0 + e] = bsum[e];
   }
 }
 
@@ -370,7 +399,7 @@ cudaError_t launch_route_backward(const Cfg& c, const void* x, const float* w_ro
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (dw_router) {
-    const dim3 grid((c.d + 63) / 64, (c.E + 63) / 64);
+    const dim3 grid((c.d + TB - 1) / TB, (c.E + DW_E - 1) / DW_E);
     if (c.act == MOE_DTYPE_F32)
       router_dw_kernel<float><<<grid, TB, 0, s>>>(dlogits, static_cast<const float*>(x),
                                                   dw_router, db_router, c.N, c.E, c.d);
