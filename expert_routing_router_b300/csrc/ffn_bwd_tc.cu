@@ -81,6 +81,7 @@ struct BwdParams {
   __nv_bfloat16* aux1;  // shared counterpart
   int* err;
   int E, n_shared, d, F, Fs;
+  int gu_send_layout;  // D1: routed g|u rows in the send-buffer layout (saved by the forward)
 };
 
 struct Ctl {
@@ -418,7 +419,9 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
               const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
               pg[i] = pack_bf16(g0, g1);
               pu[i] = pack_bf16(u0, u1);
-              ph[i] = pack_bf16(g0 / (1.0f + __expf(-g0)) * u0, g1 / (1.0f + __expf(-g1)) * u1);
+              // the forward's expression, so that recomputed h equals the saved one
+              ph[i] = pack_bf16(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                                __fdividef(g1, 1.0f + __expf(-g1)) * u1);
             }
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -437,7 +440,12 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       } else if (KIND == D1) {
         // dh columns [n0, n0+256): dg = dh u silu'(g), du = dh silu(g), from gu
         const int64_t row = tl.row_base + tl.m0 + r;
-        const __nv_bfloat16* gurow = (tl.routed ? p.aux0 : p.aux1) + row * (2 * Fx);
+        // padding rows (past the segment's rows) have dh = 0 and get zeros without
+        // reading g|u (the send-buffer layout has no such rows)
+        const bool real = tl.m0 + r < tl.M;
+        const int64_t grow =
+            ((p.gu_send_layout && tl.routed) ? tl.out_base : tl.row_base) + tl.m0 + r;
+        const __nv_bfloat16* gurow = (tl.routed ? p.aux0 : p.aux1) + grow * (2 * Fx);
         __nv_bfloat16* drow = out + row * (2 * Fx);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -449,8 +457,9 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             for (int v = 0; v < 4; ++v) {
               const int col = tl.n0 + c + v * 8;
               if (col >= Fx) continue;
-              const uint4 gv = *reinterpret_cast<const uint4*>(gurow + col);
-              const uint4 uv = *reinterpret_cast<const uint4*>(gurow + Fx + col);
+              const uint4 z4 = make_uint4(0, 0, 0, 0);
+              const uint4 gv = real ? *reinterpret_cast<const uint4*>(gurow + col) : z4;
+              const uint4 uv = real ? *reinterpret_cast<const uint4*>(gurow + Fx + col) : z4;
               const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
               const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
               uint32_t pdg[4], pdu[4];
@@ -589,9 +598,8 @@ __global__ void pad_plan_kernel(const int32_t* __restrict__ kept, int32_t* __res
 }
 
 // Rows of expert e (blockIdx.y): dst[pad_start[e] + r] = src[expert_start[e] + r] for
-// r < kept[e], zero up to the 64-row boundary; for both xperm and dY.
-__global__ void pad_rows_kernel(const uint4* __restrict__ x, const uint4* __restrict__ dy,
-                                uint4* __restrict__ xpad, uint4* __restrict__ dypad,
+// r < kept[e], zero up to the 64-row boundary.  Rows of vec 16-byte vectors.
+__global__ void pad_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                 const int32_t* __restrict__ expert_start,
                                 const int32_t* __restrict__ kept,
                                 const int32_t* __restrict__ pad_start, int vec) {
@@ -600,15 +608,8 @@ __global__ void pad_rows_kernel(const uint4* __restrict__ x, const uint4* __rest
   const int64_t src0 = expert_start[e], dst0 = pad_start[e];
   for (int r = blockIdx.x; r < npad; r += gridDim.x) {
     const int64_t so = (src0 + r) * vec, d = (dst0 + r) * vec;
-    for (int v = threadIdx.x; v < vec; v += blockDim.x) {
-      uint4 a = make_uint4(0, 0, 0, 0), b = a;
-      if (r < n) {
-        a = x[so + v];
-        b = dy[so + v];
-      }
-      xpad[d + v] = a;
-      dypad[d + v] = b;
-    }
+    for (int v = threadIdx.x; v < vec; v += blockDim.x)
+      dst[d + v] = r < n ? src[so + v] : make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -680,6 +681,10 @@ cudaError_t run(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
 // Rows of the padded routed layout: every segment rounded up to 64 rows.
 static uint64_t padded_rows(const Cfg& c) { return (uint64_t)c.send_rows + 64ull * c.E; }
 
+size_t saved_bytes(const Cfg& c) {
+  return 2 * 3 * ((size_t)c.send_rows * c.F + (size_t)c.N * c.Fs);
+}
+
 size_t ffn_backward_ws_bytes(const Cfg& c) {
   // pad_start [E+1] int32 (256 B aligned); bf16: xpad, dypad [P, d]; gu [P, 2F] +
   // [N, 2Fs]; h [P, F] + [N, Fs]; dgu [P, 2F] + [N, 2Fs]
@@ -693,8 +698,8 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
                                 const void* w_down, const void* x, const void* shared_gate_up,
                                 const void* shared_down, const void* dyperm, const void* dout,
                                 void* dxperm, void* dx_shared, void* dw_gate_up, void* dw_down,
-                                void* dshared_gate_up, void* dshared_down, void* ws, int* status,
-                                cudaStream_t s) {
+                                void* dshared_gate_up, void* dshared_down, const void* saved,
+                                void* ws, int* status, cudaStream_t s) {
   using bf = __nv_bfloat16;
   const bool sh = c.Fs > 0;
   const uint64_t N = (uint64_t)c.N, d = (uint64_t)c.d;
@@ -713,17 +718,28 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
   cudaError_t e;
   pad_plan_kernel<<<1, 256, 0, s>>>(kept_counts, pad_start, c.E);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  {
-    const dim3 grid(16, c.E);
-    pad_rows_kernel<<<grid, 256, 0, s>>>(
-        static_cast<const uint4*>(xperm), static_cast<const uint4*>(dyperm),
-        reinterpret_cast<uint4*>(xpad), reinterpret_cast<uint4*>(dypad), expert_start,
-        kept_counts, pad_start, (int)(d * 2 / 16));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  const dim3 pgrid(16, c.E);
+  auto pad = [&](const void* src, void* dst, uint64_t cols) {
+    pad_rows_kernel<<<pgrid, 256, 0, s>>>(static_cast<const uint4*>(src),
+                                          static_cast<uint4*>(dst), expert_start, kept_counts,
+                                          pad_start, (int)(cols * 2 / 16));
+    return cudaGetLastError();
+  };
+  if ((e = pad(xperm, xpad, d)) != cudaSuccess) return e;
+  if ((e = pad(dyperm, dypad, d)) != cudaSuccess) return e;
   BwdParams p{expert_start, kept_counts, pad_start, nullptr, nullptr, nullptr, nullptr, status,
-              c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
+              c.E, sh ? c.N : 0, c.d, c.F, c.Fs, 0};
   CUtensorMap a0, a1, b0, b1, o0, o1;
+  // activations kept by the forward (moe_expert_ffn_save): h [S, F] + [N, Fs], then
+  // g|u [S_send, 2F] + [N, 2Fs]; otherwise R1 recomputes them in the padded layout
+  const bf* sv_h = static_cast<const bf*>(saved);
+  const bf* sv_hs = sv_h ? sv_h + (uint64_t)c.send_rows * F : nullptr;
+  const bf* sv_gu = sv_h ? sv_hs + N * Fs : nullptr;
+  const bf* sv_gus = sv_h ? sv_gu + (uint64_t)c.send_rows * 2 * F : nullptr;
+  if (saved) {
+    if ((e = pad(sv_h, h, F)) != cudaSuccess) return e;  // W1 reads h padded
+    p.gu_send_layout = 1;
+  }
   // R1: A = padded xperm / x (K-major over d); B = W_gu rows (K-major)
   if (!make_map(&a0, xpad, d, S, 64, BM) || !make_map(&b0, w_gate_up, d, E * 2 * F, 64, BN / 2))
     return cudaErrorInvalidValue;
@@ -732,7 +748,7 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
   if (sh && (!make_map(&a1, x, d, N, 64, BM) || !make_map(&b1, shared_gate_up, d, 2 * Fs, 64, BN / 2)))
     return cudaErrorInvalidValue;
   p.out0 = gu; p.out1 = gu_s; p.aux0 = h; p.aux1 = h_s;
-  if ((e = run<R1>(a0, a1, b0, b1, a0, a0, p, s)) != cudaSuccess) return e;
+  if (!saved && (e = run<R1>(a0, a1, b0, b1, a0, a0, p, s)) != cudaSuccess) return e;
   // D1: A = padded dY (K-major over d); B = W_down as [d rows, F columns], MN-major
   if (!make_map(&a0, dypad, d, S, 64, BM) || !make_map(&b0, w_down, F, E * d, 64, 64))
     return cudaErrorInvalidValue;
@@ -740,7 +756,9 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
   b1 = b0;
   if (sh && (!make_map(&a1, dout, d, N, 64, BM) || !make_map(&b1, shared_down, Fs, d, 64, 64)))
     return cudaErrorInvalidValue;
-  p.out0 = dgu; p.out1 = dgu_s; p.aux0 = gu; p.aux1 = gu_s;
+  p.out0 = dgu; p.out1 = dgu_s;
+  p.aux0 = saved ? const_cast<bf*>(sv_gu) : gu;
+  p.aux1 = saved ? const_cast<bf*>(sv_gus) : gu_s;
   if ((e = run<D1>(a0, a1, b0, b1, a0, a0, p, s)) != cudaSuccess) return e;
   // D2: A = [dG | dU] (K-major over 2F); B = W_gu as [2F rows, d columns], MN-major
   if (!make_map(&a0, dgu, 2 * F, S, 64, BM) || !make_map(&b0, w_gate_up, d, E * 2 * F, 64, 64))
@@ -757,7 +775,8 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
-  if (sh && (!make_map(&a1, dout, d, N, 64, 64) || !make_map(&b1, h_s, Fs, N, 64, 64)))
+  if (sh && (!make_map(&a1, dout, d, N, 64, 64) ||
+             !make_map(&b1, saved ? sv_hs : h_s, Fs, N, 64, 64)))
     return cudaErrorInvalidValue;
   // dWd [E, d, F] and the shared [d, Fs], written by TMA stores
   if (!make_out_map(&o0, dw_down, F, d, E)) return cudaErrorInvalidValue;

@@ -61,6 +61,8 @@ struct TcParams {
   int* err;
   int E, n_shared, d, F, Fs;
   int stall_cta;  // self-test only: this CTA arms its first ring slot without loading it
+  __nv_bfloat16* gu0;  // optional (training): g and u of each routed row, [rows, 2F]
+  __nv_bfloat16* gu1;  // and of the shared expert, [N, 2Fs]
 };
 
 struct Ctl {
@@ -353,6 +355,26 @@ grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_consta
                 *reinterpret_cast<uint4*>(orow + col) =
                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
+            __nv_bfloat16* gubase = routed ? p.gu0 : p.gu1;
+            if (gubase) {  // training: keep g and u for the backward pass
+              __nv_bfloat16* gurow = gubase + (int64_t)(tl.row_base + tl.m0 + r) * (2 * ncols);
+              uint32_t pg[16], pu[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                pg[i] = pack_bf16(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+                pu[i] = pack_bf16(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+              }
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int col = tl.n0 + c + v * 8;
+                if (col < ncols) {
+                  *reinterpret_cast<uint4*>(gurow + col) =
+                      make_uint4(pg[4 * v], pg[4 * v + 1], pg[4 * v + 2], pg[4 * v + 3]);
+                  *reinterpret_cast<uint4*>(gurow + ncols + col) =
+                      make_uint4(pu[4 * v], pu[4 * v + 1], pu[4 * v + 2], pu[4 * v + 3]);
+                }
+              }
+            }
           }
         }
       } else {
@@ -428,7 +450,7 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,
                           void* yperm, void* yshared, void* h, int* status, cudaStream_t s,
-                          int stall_cta) {
+                          int stall_cta, void* gu_save) {
   const bool sh = c.Fs > 0;
   __nv_bfloat16* h_routed = static_cast<__nv_bfloat16*>(h);
   __nv_bfloat16* h_shared = h_routed + (size_t)c.send_rows * c.F;
@@ -440,8 +462,10 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
   b1 = b0;
   if (sh && (!make_map(&a1, x, c.d, c.N, BM) || !make_map(&b1, shared_gate_up, c.d, 2 * c.Fs, BN / 2)))
     return cudaErrorInvalidValue;
+  __nv_bfloat16* gu_routed = static_cast<__nv_bfloat16*>(gu_save);
+  __nv_bfloat16* gu_shared = gu_routed ? gu_routed + (size_t)c.send_rows * 2 * c.F : nullptr;
   TcParams p{expert_start, kept_counts, h_routed, h_shared, status,
-             c.E, sh ? c.N : 0, c.d, c.F, c.Fs, stall_cta};
+             c.E, sh ? c.N : 0, c.d, c.F, c.Fs, stall_cta, gu_routed, sh ? gu_shared : nullptr};
   const int grid = num_sms();
   auto k1 = grouped_ffn_kernel<GATE_UP>;
   auto k2 = grouped_ffn_kernel<DOWN>;
@@ -466,6 +490,7 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
   p.out0 = static_cast<__nv_bfloat16*>(yperm);
   p.out1 = static_cast<__nv_bfloat16*>(yshared);
   p.stall_cta = -1;  // only the first GEMM takes part in the self-test
+  p.gu0 = p.gu1 = nullptr;
   k2<<<grid, THREADS, SMEM_BYTES, s>>>(a0, a1, b0, b1, p);
   return cudaGetLastError();
 }

@@ -143,7 +143,8 @@ moe_status expert_ffn_impl(const moe_config* cfg, const void* xperm, const int32
                            const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                            const void* x, const void* shared_gate_up, const void* shared_down,
                            void* yperm, void* yshared, void* workspace, size_t workspace_bytes,
-                           void* stream, int stall_cta) {
+                           void* stream, int stall_cta, void* saved = nullptr,
+                           size_t saved_size = 0) {
   Cfg c;
   moe_status st = make_cfg(cfg, &c);
   if (st != MOE_OK) return st;
@@ -164,6 +165,16 @@ moe_status expert_ffn_impl(const moe_config* cfg, const void* xperm, const int32
   int* status = reinterpret_cast<int*>(static_cast<char*>(workspace) + w.status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const void* xs = c.Fs > 0 ? x : nullptr;
+  if (saved) {  // training forward: h and g|u go to the caller's buffer (prefill kernels)
+    if (c.act != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (!aligned(saved, 16)) return MOE_ERR_INVALID_ARG;
+    if (saved_size < saved_bytes(c)) return MOE_ERR_WORKSPACE;
+    __nv_bfloat16* hs = static_cast<__nv_bfloat16*>(saved);
+    __nv_bfloat16* gus = hs + (size_t)c.send_rows * c.F + (size_t)c.N * c.Fs;
+    return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
+                                   shared_gate_up, shared_down, yperm, yshared, hs, status, s,
+                                   -1, gus));
+  }
   if (stall_cta >= 0) {
     if (c.act != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
     return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
@@ -298,6 +309,27 @@ moe_status moe_selftest_ffn_stall(const moe_config* cfg, const void* xperm,
                          stream, 0);
 }
 
+moe_status moe_saved_size(const moe_config* cfg, size_t* bytes) {
+  Cfg c;
+  moe_status st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = saved_bytes(c);
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn_save(const moe_config* cfg, const void* xperm,
+                               const int32_t* expert_start, const int32_t* kept_counts,
+                               const void* w_gate_up, const void* w_down, const void* x,
+                               const void* shared_gate_up, const void* shared_down, void* yperm,
+                               void* yshared, void* saved, size_t saved_size, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!saved) return MOE_ERR_INVALID_ARG;
+  return expert_ffn_impl(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
+                         shared_gate_up, shared_down, yperm, yshared, workspace, workspace_bytes,
+                         stream, -1, saved, saved_size);
+}
+
 moe_status moe_combine(const moe_config* cfg, const void* yperm, const int32_t* slot_of,
                        const float* topk_w, const void* residual, const void* yshared, void* out,
                        void* stream) {
@@ -426,8 +458,8 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xperm,
                                    const void* shared_gate_up, const void* shared_down,
                                    const void* dyperm, const void* dout, void* dxperm,
                                    void* dx_shared, void* dw_gate_up, void* dw_down,
-                                   void* dshared_gate_up, void* dshared_down, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+                                   void* dshared_gate_up, void* dshared_down, const void* saved,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
   Cfg c;
   moe_status st = make_cfg(cfg, &c);
   if (st != MOE_OK) return st;
@@ -443,6 +475,7 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xperm,
     for (const void* q : sh)
       if (!q || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
   }
+  if (saved && !aligned(saved, 16)) return MOE_ERR_INVALID_ARG;
   size_t need = 0;
   if ((st = moe_backward_workspace_size(cfg, &need)) != MOE_OK) return st;
   if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
@@ -452,8 +485,8 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xperm,
   return from_cuda(launch_ffn_backward(c, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
                                        shared_gate_up, shared_down, dyperm, dout, dxperm,
                                        dx_shared, dw_gate_up, dw_down, dshared_gate_up,
-                                       dshared_down, static_cast<char*>(workspace) + 256, status,
-                                       static_cast<cudaStream_t>(stream)));
+                                       dshared_down, saved, static_cast<char*>(workspace) + 256,
+                                       status, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_route_backward(const moe_config* cfg, const void* x, const float* w_router,

@@ -102,7 +102,7 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
                           const void* x, const void* shared_gate_up, const void* shared_down,
                           void* yperm, void* yshared, void* h, int* status, cudaStream_t s,
-                          int stall_cta = -1);
+                          int stall_cta = -1, void* gu_save = nullptr);
 cudaError_t launch_ffn_tc_small(const Cfg& c, const void* xperm, const int32_t* expert_start,
                                 const int32_t* kept_counts, const void* w_gate_up,
                                 const void* w_down, const void* x, const void* shared_gate_up,
@@ -151,7 +151,10 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
                                 const void* w_down, const void* x, const void* shared_gate_up,
                                 const void* shared_down, const void* dyperm, const void* dout,
                                 void* dxperm, void* dx_shared, void* dw_gate_up, void* dw_down,
-                                void* dshared_gate_up, void* dshared_down, void* ws, int* status,
-                                cudaStream_t s);
+                                void* dshared_gate_up, void* dshared_down, const void* saved,
+                                void* ws, int* status, cudaStream_t s);
+// Bytes of the activations a training forward keeps for the backward:
+// h [S, F] + [N, Fs], then g|u [S, 2F] + [N, 2Fs], bf16.
+size_t saved_bytes(const Cfg& c);
 int num_sms();
 }  // namespace moe

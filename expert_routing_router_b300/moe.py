@@ -39,6 +39,7 @@ EXPORTS = ("moe_send_rows", "moe_workspace_size", "moe_route", "moe_dispatch", "
            "moe_expert_ffn", "moe_selftest_ffn_stall", "moe_combine", "moe_bias_update",
            "moe_dispatch_q8", "moe_quant_rows", "moe_dequant_rows", "moe_combine_q8",
            "moe_backward_workspace_size", "moe_combine_backward", "moe_expert_ffn_backward",
+           "moe_saved_size", "moe_expert_ffn_save",
            "moe_route_backward", "moe_dispatch_backward", "moe_status_string")
 
 
@@ -64,7 +65,9 @@ def _load():
     lib.moe_combine_q8.argtypes = [C] + [P] * 7 + [P]
     lib.moe_backward_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_combine_backward.argtypes = [C] + [P] * 6 + [P]
-    lib.moe_expert_ffn_backward.argtypes = [C] + [P] * 17 + [S, P]
+    lib.moe_expert_ffn_backward.argtypes = [C] + [P] * 18 + [S, P]
+    lib.moe_saved_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_expert_ffn_save.argtypes = [C] + [P] * 11 + [S, P, S, P]
     lib.moe_route_backward.argtypes = [C] + [P] * 9 + [P]
     lib.moe_dispatch_backward.argtypes = [C] + [P] * 6 + [P]
     lib.moe_status_string.argtypes = [I]
@@ -221,13 +224,30 @@ def moe_combine_backward(cfg, dout, yperm, slot_of, topk_w, dyperm, dtopk_w, str
 def moe_expert_ffn_backward(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
                             shared_gate_up, shared_down, dyperm, dout, dxperm, dx_shared,
                             dw_gate_up, dw_down, dshared_gate_up, dshared_down, workspace,
-                            stream=None):
+                            stream=None, saved=None):
     _check("moe_expert_ffn_backward", _lib.moe_expert_ffn_backward(
         ctypes.byref(cfg), _p(xperm), _p(expert_start), _p(kept_counts), _p(w_gate_up),
         _p(w_down), _p(x), _p(shared_gate_up), _p(shared_down), _p(dyperm), _p(dout),
         _p(dxperm), _p(dx_shared), _p(dw_gate_up), _p(dw_down), _p(dshared_gate_up),
-        _p(dshared_down), _p(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+        _p(dshared_down), _p(saved), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_saved_size(cfg):
+    n = ctypes.c_size_t(0)
+    _check("moe_saved_size", _lib.moe_saved_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def moe_expert_ffn_save(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down, x,
+                        shared_gate_up, shared_down, yperm, yshared, saved, workspace,
+                        stream=None):
+    """moe_expert_ffn that also keeps h and g|u in `saved` for the backward pass."""
+    _check("moe_expert_ffn_save", _lib.moe_expert_ffn_save(
+        ctypes.byref(cfg), _p(xperm), _p(expert_start), _p(kept_counts), _p(w_gate_up),
+        _p(w_down), _p(x), _p(shared_gate_up), _p(shared_down), _p(yperm), _p(yshared),
+        _p(saved), saved.numel() * saved.element_size(), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def moe_route_backward(cfg, x, w_router, logits, topk_idx, dtopk_w, dlogits, dx_router,
@@ -271,16 +291,17 @@ class GradBuffers:
         self.workspace[:256].zero_()          # sticky device status word starts at 0
 
 
-def run_layer_backward(b, g, inp, dout, stream=None):
+def run_layer_backward(b, g, inp, dout, stream=None, saved=None):
     """Backward of the layer pass held in LayerBuffers b (selection fixed), from dout:
-    combine, expert FFN (recompute, dgrad, wgrad), router, dispatch.  Writes every
-    gradient into GradBuffers g and returns g.dx."""
+    combine, expert FFN (dgrad, wgrad; g, u and h from `saved` if the forward kept them
+    with moe_expert_ffn_save, else recomputed), router, dispatch.  Writes every gradient
+    into GradBuffers g and returns g.dx."""
     c = b.cfg
     moe_combine_backward(c, dout, b.yperm, b.slot_of, b.topk_w, g.dyperm, g.dtopk_w, stream)
     moe_expert_ffn_backward(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
                             inp["w_down"], inp["x"], inp["shared_gate_up"], inp["shared_down"],
                             g.dyperm, dout, g.dxperm, g.dx_shared, g.dw_gate_up, g.dw_down,
-                            g.dshared_gate_up, g.dshared_down, g.workspace, stream)
+                            g.dshared_gate_up, g.dshared_down, g.workspace, stream, saved)
     moe_route_backward(c, inp["x"], inp["w_router"], b.logits, b.topk_idx, g.dtopk_w, g.dlogits,
                        g.dx_router, g.dw_router, g.db_router, stream)
     moe_dispatch_backward(c, g.dxperm, b.slot_of, dout, g.dx_shared, g.dx_router, g.dx, stream)
@@ -333,7 +354,7 @@ def with_tokens(cfg, tokens):
     return c
 
 
-def layer_parts(b, inp, bias_step=0.0, stream=None, replicas=1):
+def layer_parts(b, inp, bias_step=0.0, stream=None, replicas=1, saved=None):
     """The layer step as three stream-ordered parts: (1) route and dispatch, (2) expert
     FFN and combine, (3) the bias update (None when there is none).  With an INT8
     payload (LayerBuffers of a workload with payload="int8") the send and return
@@ -357,9 +378,15 @@ def layer_parts(b, inp, bias_step=0.0, stream=None, replicas=1):
                          b.num_kept, b.workspace, stream)
 
     def compute_return():
-        moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
-                       inp["w_down"], inp["x"], inp["shared_gate_up"], inp["shared_down"],
-                       b.yperm, b.yshared, b.workspace, stream)
+        if saved is not None:   # training: keep h and g|u for the backward
+            moe_expert_ffn_save(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
+                                inp["w_down"], inp["x"], inp["shared_gate_up"],
+                                inp["shared_down"], b.yperm, b.yshared, saved, b.workspace,
+                                stream)
+        else:
+            moe_expert_ffn(c, b.xperm, b.expert_start, b.kept_counts, inp["w_gate_up"],
+                           inp["w_down"], inp["x"], inp["shared_gate_up"], inp["shared_down"],
+                           b.yperm, b.yshared, b.workspace, stream)
         if b.int8_payload:
             moe_quant_rows(c, b.yperm, b.perm_src, b.yperm_q, b.yscale, stream)
             moe_combine_q8(c, b.yperm_q, b.yscale, b.slot_of, b.topk_w, inp["x"], b.yshared,
@@ -376,7 +403,7 @@ def layer_parts(b, inp, bias_step=0.0, stream=None, replicas=1):
     return send, compute_return, update
 
 
-def run_layer(b, inp, bias_step=0.0, stream=None, reduce_counts=None, replicas=1):
+def run_layer(b, inp, bias_step=0.0, stream=None, reduce_counts=None, replicas=1, saved=None):
     """One pass of the layer path through the C ABI: route, dispatch, expert FFN,
     combine, and (if bias_step) the selection-bias update (see layer_parts).
 
@@ -385,8 +412,10 @@ def run_layer(b, inp, bias_step=0.0, stream=None, reduce_counts=None, replicas=1
     routed counts over the replicas in place (an all-reduce; it may return a handle
     whose .wait() orders it before the bias update, so that it overlaps the expert
     FFN), and the sign rule then compares the summed counts with the mean load of all
-    `replicas` batches.  b.expert_counts holds the summed counts afterwards."""
-    send, compute_return, update = layer_parts(b, inp, bias_step, stream, replicas)
+    `replicas` batches.  b.expert_counts holds the summed counts afterwards.  With
+    `saved` (moe_saved_size bytes) the expert FFN also keeps its activations there for
+    run_layer_backward."""
+    send, compute_return, update = layer_parts(b, inp, bias_step, stream, replicas, saved)
     send()
     handle = None
     if update is not None and reduce_counts is not None:

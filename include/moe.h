@@ -309,8 +309,23 @@ MOE_API moe_status moe_combine_q8(const moe_config* cfg, const int8_t* yperm_q, 
  * The forward's own buffers (logits, topk_idx, topk_w, slot_of, expert_start,
  * kept_counts, xperm, yperm) are the inputs; they must be those of the same call. */
 
-/* Bytes of the workspace moe_expert_ffn_backward needs (status word + recomputed
- * gate/up and h, and [dg | du], bf16). */
+/* Bytes of the activations a training forward keeps for the backward:
+ * h [S, F] + [N, Fs], then g|u [S, 2F] + [N, 2Fs], bf16 (S = moe_send_rows). */
+MOE_API moe_status moe_saved_size(const moe_config* cfg, size_t* bytes);
+
+/* moe_expert_ffn for training: the same outputs, and the SwiGLU activations h and the
+ * gate/up pre-activations g|u of every row written to `saved` (moe_saved_size bytes,
+ * 16-byte aligned), so that moe_expert_ffn_backward need not recompute them.  bf16
+ * layers only (fp32: MOE_ERR_UNSUPPORTED); always the prefill tensor-core kernels. */
+MOE_API moe_status moe_expert_ffn_save(const moe_config* cfg, const void* xperm,
+                                       const int32_t* expert_start, const int32_t* kept_counts,
+                                       const void* w_gate_up, const void* w_down, const void* x,
+                                       const void* shared_gate_up, const void* shared_down,
+                                       void* yperm, void* yshared, void* saved, size_t saved_bytes,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of the workspace moe_expert_ffn_backward needs (status word, the padded copies
+ * of the send rows and of dY, the gate/up and h activations and [dg | du], bf16). */
 MOE_API moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Combine backward.  Same page, step 4, differentiated: for each kept choice,
@@ -338,6 +353,8 @@ MOE_API moe_status moe_combine_backward(const moe_config* cfg, const void* dout,
  *   dw_gate_up [E, 2F, hidden], dw_down [E, hidden, F]  out (experts with no kept rows
  *                       get zeros); dshared_gate_up [2Fs, hidden], dshared_down
  *                       [hidden, Fs] out (NULL without a shared expert)
+ *   saved               the activations moe_expert_ffn_save kept in the forward of the
+ *                       same layer call, or NULL to recompute g, u and h here
  *   workspace           moe_backward_workspace_size bytes, 256-byte aligned; its
  *                       first int32 is a sticky status word (caller zeroes it; nonzero
  *                       if a kernel gave up a bounded wait). */
@@ -348,7 +365,8 @@ MOE_API moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xp
                                            const void* dyperm, const void* dout, void* dxperm,
                                            void* dx_shared, void* dw_gate_up, void* dw_down,
                                            void* dshared_gate_up, void* dshared_down,
-                                           void* workspace, size_t workspace_bytes, void* stream);
+                                           const void* saved, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
 /* Router backward.  The combine weights as functions of the logits (moe_route):
  *   softmax, renormalised:   dl_j = w_j (dw_j - sum_i w_i dw_i) on the selection, 0 off it

@@ -153,7 +153,7 @@ def test_backward_calls_validate_on_host(moe_lib):
     assert need >= 2 * 5 * (8192 * 8 * 2048 + 8192 * 2048)
     c0 = moe_lib.config(W.TINY_TOP2_F32)
     n0 = moe_lib.moe_backward_workspace_size(c0)
-    args = [P(FAKE)] * 16               # every pointer before the workspace
+    args = [P(FAKE)] * 16 + [None]      # every pointer before the workspace; no saved
     assert L.moe_expert_ffn_backward(ctypes.byref(c0), *args, P(FAKE), n0, None) == \
         moe_lib.MOE_ERR_UNSUPPORTED
     assert L.moe_expert_ffn_backward(ctypes.byref(c3), *args, P(FAKE), need - 1, None) == \

@@ -41,14 +41,24 @@ def rows_of(t, idx):
     return t[torch.as_tensor(np.asarray(idx, np.int64), device=t.device)]
 
 
-def run_backward(w, inp, seed=0):
+def run_backward(w, inp, seed=0, save=False):
+    """Forward then backward; with save=True the forward keeps h and g|u
+    (moe_expert_ffn_save) and the backward reuses them instead of recomputing."""
     from expert_routing_router_b300 import moe
-    b, _ = P.run_gpu(w, inp)
+    saved = None
+    if save:
+        b = moe.LayerBuffers(w)
+        saved = torch.empty(moe.moe_saved_size(b.cfg), dtype=torch.uint8, device="cuda")
+        moe.run_layer(b, inp, saved=saved)
+        torch.cuda.synchronize()
+        assert int(b.workspace[:4].view(torch.int32).item()) == 0
+    else:
+        b, _ = P.run_gpu(w, inp)
     g = moe.GradBuffers(w)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(1000 + seed)
     dout = torch.randn(w.tokens, w.hidden, generator=gen, device="cuda").to(w.torch_dtype)
-    moe.run_layer_backward(b, g, inp, dout)
+    moe.run_layer_backward(b, g, inp, dout, saved=saved)
     torch.cuda.synchronize()
     assert int(g.workspace[:4].view(torch.int32).item()) == 0, "backward status word set"
     return b, g, dout
@@ -232,3 +242,33 @@ def test_backward_graph_replay_bit_exact():
     torch.cuda.synchronize()
     for a, r in zip((g.dx, g.dw_gate_up, g.dw_down, g.dw_router), ref):
         assert torch.equal(a, r)
+
+
+@pytest.mark.parametrize("name", ["sigmoid_groups_shared", "long_segments", "softmax_norm_padded"])
+def test_backward_with_saved_activations(name):
+    """Training forward (moe_expert_ffn_save) + backward reusing its h and g|u: full
+    parity, and the same gradients as the recomputing backward (same kernels, same
+    accumulation order)."""
+    w = BWD_EDGE[name]
+    inp = W.make_inputs(w, seed=23, device="cuda")
+    b, g, dout = run_backward(w, inp, save=True)
+    check_backward(w, inp, b, g, dout, n_tok=None if w.tokens <= 1000 else 96)
+    b2, g2, dout2 = run_backward(w, inp, save=False)
+    assert torch.equal(dout, dout2)
+    for name_ in ("dx", "dw_gate_up", "dw_down", "dxperm"):
+        a, r = getattr(g, name_), getattr(g2, name_)
+        if name_ == "dxperm":
+            rows = torch.from_numpy(np.nonzero(P.host(b.perm_src) >= 0)[0]).cuda()
+            a, r = a[rows], r[rows]
+        assert torch.equal(a, r), name_
+
+
+def test_backward_dsv3_prefill_saved(dsv3_inputs):
+    w, (inp, hw) = W.DSV3_PREFILL, dsv3_inputs
+    b, g, dout = run_backward(w, inp, save=True)
+    counts = P.host(b.kept_counts)
+    nz = np.nonzero(counts)[0]
+    check_backward(w, inp, b, g, dout, n_tok=8, n_rows=24,
+                   experts=[int(nz[np.argmax(counts[nz])])], n_f=4, hw=hw)
+    del b, g
+    torch.cuda.empty_cache()
