@@ -46,7 +46,8 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int OUT_BYTES = BM * BN * 2;  // W kinds: one bf16 output tile staged for TMA stores
+constexpr int OUT_BYTES = BM * 64 * 2;  // W kinds: one 64-column box of the output tile,
+                                        // staged for a TMA store (four rounds per tile)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -64,9 +65,9 @@ struct Traits {
   static constexpr bool b_mn = KIND != R1;                  // B loaded MN-major
   static constexpr bool k_rows = KIND == W1 || KIND == W2;  // reduction over segment rows
   // W kinds: short K loops (a segment's rows) make the output write the critical path;
-  // the tile goes out through shared memory and TMA stores, which costs one ring stage
+  // the tile goes out through a 16 KB shared-memory box and TMA stores
   static constexpr bool tma_out = k_rows;
-  static constexpr int stages = tma_out ? 3 : STAGES;
+  static constexpr int stages = STAGES;
   static constexpr uint32_t idesc =
       idesc_bf16_f32(BM, BN) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
 };
@@ -192,9 +193,18 @@ __device__ __forceinline__ Tile decode(const Ctl* ctl, int nseg, int t, const Bw
   tl.routed = lo < p.E;
   extents<KIND>(tl.routed, ctl->rows[lo], p, &tl.M, &tl.N, &tl.K);
   const int local = t - ctl->tile_start[lo];
-  const int mt = ctl->mtiles[lo];
-  tl.m0 = (local % mt) * BM;
-  tl.n0 = (local / mt) * n_step<KIND>();
+  if (Traits<KIND>::k_rows) {
+    // W kinds: column tiles fastest, so that the CTAs running at the same time write
+    // whole contiguous rows of dW (the write stream is the bound there)
+    const int nt = (tl.N + n_step<KIND>() - 1) / n_step<KIND>();
+    tl.m0 = (local / nt) * BM;
+    tl.n0 = (local % nt) * n_step<KIND>();
+  } else {
+    // column-tile major: CTAs running at the same time share a weight tile in L2
+    const int mt = ctl->mtiles[lo];
+    tl.m0 = (local % mt) * BM;
+    tl.n0 = (local / mt) * n_step<KIND>();
+  }
   tl.row_base = ctl->row_base[lo];
   tl.out_base = ctl->out_base[lo];
   return tl;
@@ -485,51 +495,46 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           }
         }
       } else if (Tr::tma_out) {
-        // [M, N] tile of dW -> shared memory (four 64-column boxes, 128-byte swizzle:
-        // 16-byte chunk j of row r at r*128 + (j ^ (r & 7))*16) -> TMA stores.  The
-        // previous tile's stores must have read the buffer first.
-        if (threadIdx.x == 64) bulk_wait_read();
-        if (!epi_sync(ctl, &esync_phase, p.err)) break;
-        // four 32-column TMEM loads in flight per wait (the K loops are short, so the
-        // load latency is not hidden behind the next tile's MMAs)
+        // [M, N] tile of dW, one 64-column box at a time: TMEM -> registers -> the 16 KB
+        // staging box (128-byte swizzle: 16-byte chunk j of row r at r*128 + (j^(r&7))*16)
+        // -> one TMA store.  Before writing the box, the previous store must have read it.
+        bool ok = true;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 128) {
-          uint32_t y[4][32];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tb + c0 + 32 * q4, y[q4]);
+        for (int bx = 0; bx < BN / 64 && ok; ++bx) {
+          uint32_t y[2][32];
+          tmem_ld32(tb + 64 * bx, y[0]);
+          tmem_ld32(tb + 64 * bx + 32, y[1]);
           tmem_ld_wait(y[0]);
+          tmem_regs_ready(y[1]);
+          if (bx == BN / 64 - 1) {  // the accumulator goes back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
+          }
+          if (threadIdx.x == 64) bulk_wait_read();
+          if (!epi_sync(ctl, &esync_phase, p.err)) { ok = false; break; }
 #pragma unroll
-          for (int q4 = 1; q4 < 4; ++q4) tmem_regs_ready(y[q4]);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16(__uint_as_float(y[q4][2 * i]), __uint_as_float(y[q4][2 * i + 1]));
+              pk[i] = pack_bf16(__uint_as_float(y[h2][2 * i]), __uint_as_float(y[h2][2 * i + 1]));
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              const int col = c0 + 32 * q4 + v * 8;
-              const int box = col >> 6, chunk = (col & 63) >> 3;
-              *reinterpret_cast<uint4*>(stage_out + box * (BM * 128) + r * 128 +
-                                        ((chunk ^ (r & 7)) << 4)) =
+              const int chunk = h2 * 4 + v;
+              *reinterpret_cast<uint4*>(stage_out + r * 128 + ((chunk ^ (r & 7)) << 4)) =
                   make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
           }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          if (!epi_sync(ctl, &esync_phase, p.err)) { ok = false; break; }
+          if (threadIdx.x == 64 && tl.n0 + 64 * bx < tl.N) {
+            tma_store_3d(tl.routed ? &tmO0 : &tmO1, stage_out, tl.n0 + 64 * bx, tl.m0,
+                         tl.routed ? tl.seg : 0);
+            bulk_commit();
+          }
         }
-        // the accumulator can go back to the MMA warp before the stores
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (!epi_sync(ctl, &esync_phase, p.err)) break;
-        if (threadIdx.x == 64) {
-          const CUtensorMap* mo = tl.routed ? &tmO0 : &tmO1;
-          const int z = tl.routed ? tl.seg : 0;
-          for (int b = 0; b < BN / 64; ++b)
-            if (tl.n0 + 64 * b < tl.N)
-              tma_store_3d(mo, stage_out + b * (BM * 128), tl.n0 + 64 * b, tl.m0, z);
-          bulk_commit();
-        }
+        if (!ok) break;
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
         continue;
