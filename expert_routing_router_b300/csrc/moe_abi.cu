@@ -171,6 +171,10 @@ moe_status expert_ffn_impl(const moe_config* cfg, const void* xperm, const int32
     if (saved_size < saved_bytes(c)) return MOE_ERR_WORKSPACE;
     __nv_bfloat16* hs = static_cast<__nv_bfloat16*>(saved);
     __nv_bfloat16* gus = hs + (size_t)c.send_rows * c.F + (size_t)c.N * c.Fs;
+    if (c.A >= (int64_t)kPairRowsPerExpert * c.E)
+      return from_cuda(launch_ffn_tc2(c, xperm, expert_start, kept_counts, w_gate_up, w_down,
+                                      xs, shared_gate_up, shared_down, yperm, yshared, hs, status,
+                                      s, gus));
     return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
                                    shared_gate_up, shared_down, yperm, yshared, hs, status, s,
                                    -1, gus));
@@ -189,6 +193,11 @@ moe_status expert_ffn_impl(const moe_config* cfg, const void* xperm, const int32
     return from_cuda(launch_ffn_tc_small(c, xperm, expert_start, kept_counts, w_gate_up, w_down,
                                          xs, shared_gate_up, shared_down, yperm, yshared, h,
                                          status, s));
+  // many rows per expert: 256-row tiles on SM pairs (half the weight stream per SM);
+  // otherwise 128-row tiles on single SMs (less padding of each expert's last tile)
+  if (c.A >= (int64_t)kPairRowsPerExpert * c.E)
+    return from_cuda(launch_ffn_tc2(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
+                                    shared_gate_up, shared_down, yperm, yshared, h, status, s));
   return from_cuda(launch_ffn_tc(c, xperm, expert_start, kept_counts, w_gate_up, w_down, xs,
                                  shared_gate_up, shared_down, yperm, yshared, h, status, s));
 }

@@ -103,6 +103,12 @@ cudaError_t launch_ffn_tc(const Cfg& c, const void* xperm, const int32_t* expert
                           const void* x, const void* shared_gate_up, const void* shared_down,
                           void* yperm, void* yshared, void* h, int* status, cudaStream_t s,
                           int stall_cta = -1, void* gu_save = nullptr);
+// The same two GEMMs on SM pairs (tcgen05 cta_group::2, ffn_tc2.cu): the prefill path.
+cudaError_t launch_ffn_tc2(const Cfg& c, const void* xperm, const int32_t* expert_start,
+                           const int32_t* kept_counts, const void* w_gate_up, const void* w_down,
+                           const void* x, const void* shared_gate_up, const void* shared_down,
+                           void* yperm, void* yshared, void* h, int* status, cudaStream_t s,
+                           void* gu_save = nullptr);
 cudaError_t launch_ffn_tc_small(const Cfg& c, const void* xperm, const int32_t* expert_start,
                                 const int32_t* kept_counts, const void* w_gate_up,
                                 const void* w_down, const void* x, const void* shared_gate_up,
@@ -114,6 +120,13 @@ cudaError_t launch_ffn_tc_small(const Cfg& c, const void* xperm, const int32_t* 
 #define MOE_SMALL_ROWS 4
 #endif
 constexpr int kSmallRowsPerExpert = MOE_SMALL_ROWS;
+// Average send-buffer rows per expert from which the SM-pair kernels (256-row tiles)
+// are used for the expert FFN: below it, padding every expert's last tile to 256 rows
+// costs more than the pair saves on the weight stream.
+#ifndef MOE_PAIR_ROWS
+#define MOE_PAIR_ROWS 512
+#endif
+constexpr int kPairRowsPerExpert = MOE_PAIR_ROWS;
 cudaError_t launch_combine(const Cfg& c, const void* yperm, const int32_t* slot_of,
                            const float* topk_w, const void* residual, const void* yshared,
                            void* out, cudaStream_t s);

@@ -399,6 +399,15 @@ EDGE = {
     "minimal_sizes_f32": small(tokens=5, hidden=8, num_experts=4, top_k=2, num_ranks=2,
                                score_fn=0, num_groups=1, topk_groups=1, d_ff=8, shared_d_ff=8,
                                act_dtype="f32", sel_bias_std=0.0),
+    # at least 512 send rows per expert: the SM-pair (cta_group::2) expert kernels,
+    # ragged hidden / d_ff, one expert's rows not a multiple of 256, shared expert
+    "pair_kernel_ragged_shared": small(tokens=1500, hidden=264, num_experts=4, top_k=2,
+                                       num_ranks=2, num_groups=2, topk_groups=1, d_ff=200,
+                                       shared_d_ff=72),
+    "pair_kernel_softmax_capacity": small(tokens=2100, hidden=136, num_experts=6, top_k=3,
+                                          num_ranks=3, score_fn=0, num_groups=1, topk_groups=1,
+                                          capacity_factor=1.1, d_ff=392, shared_d_ff=0,
+                                          sel_bias_std=0.0),
     "capacity_exact_boundary": small(tokens=256, hidden=64, num_experts=4, top_k=1, num_ranks=4,
                                      score_fn=0, num_groups=1, topk_groups=1,
                                      capacity_factor=1.0, d_ff=32, shared_d_ff=0,
