@@ -294,6 +294,55 @@ select_kernel(const float* __restrict__ partial, int nsplit, int Epad, const flo
 
 }  // namespace
 
+// Few tokens (decode): logits straight from the fp32 weight on the CUDA cores.  One
+// CTA per expert keeps its slice of that expert's weight row in registers and runs it
+// against every token (at most kSmallRouteTokens), fp32 FMAs, then a fixed-order block
+// sum; the partial-logit layout is the tensor-core path's with one slice, so the same
+// select_kernel adds the bias and selects.  The weight is read once and nothing is
+// re-split per call (the tensor-core path rewrites the 3-term bf16 split every call).
+constexpr int kSmallRouteTokens = 16;
+
+__global__ void __launch_bounds__(THREADS)
+route_small_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
+                   float* __restrict__ partial, int N, int d, int Epad) {
+  __shared__ float red[THREADS / 32][kSmallRouteTokens];
+  const int e = blockIdx.x;
+  const int units = d / 8;
+  float acc[kSmallRouteTokens];
+#pragma unroll
+  for (int t = 0; t < kSmallRouteTokens; ++t) acc[t] = 0.0f;
+  for (int u = threadIdx.x; u < units; u += THREADS) {
+    const float4* wp = reinterpret_cast<const float4*>(W + (int64_t)e * d) + 2 * u;
+    const float4 w0 = wp[0], w1 = wp[1];
+    const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int t = 0; t < kSmallRouteTokens; ++t) {
+      if (t >= N) break;
+      const uint4 v = reinterpret_cast<const uint4*>(x + (int64_t)t * d)[u];
+      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[t] = fmaf(w[2 * i], __uint_as_float(q[i] << 16), acc[t]);
+        acc[t] = fmaf(w[2 * i + 1], __uint_as_float(q[i] & 0xffff0000u), acc[t]);
+      }
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int t = 0; t < kSmallRouteTokens; ++t) {
+    float v = acc[t];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) red[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < N) {
+    float v = 0.0f;
+    for (int w8 = 0; w8 < THREADS / 32; ++w8) v += red[w8][threadIdx.x];
+    partial[(int64_t)threadIdx.x * Epad + e] = v;
+  }
+}
+
 cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, const float* b_router,
                          const float* sel_bias, float* logits, int32_t* topk_idx, float* topk_w,
                          void* ws_split, float* partial, int* status, cudaStream_t s) {
@@ -311,13 +360,21 @@ cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, con
                                      logits, topk_idx, topk_w, p);
     return cudaGetLastError();
   }
-  // bf16 hidden states: tensor-core GEMM over the 3-term bf16 split of the weight
   const RouterPlan rp = router_plan(c);
-  cudaError_t e = launch_router_gemm(c, rp, x, w_router, ws_split, partial, status, s);
-  if (e != cudaSuccess) return e;
+  int nsplit = rp.nsplit;
+  if (c.N <= kSmallRouteTokens) {
+    // decode-sized batches: fp32 dot products on the CUDA cores, one slice
+    route_small_kernel<<<c.E, THREADS, 0, s>>>(static_cast<const __nv_bfloat16*>(x), w_router,
+                                                partial, c.N, c.d, rp.Epad);
+    nsplit = 1;
+  } else {
+    // bf16 hidden states: tensor-core GEMM over the 3-term bf16 split of the weight
+    cudaError_t e = launch_router_gemm(c, rp, x, w_router, ws_split, partial, status, s);
+    if (e != cudaSuccess) return e;
+  }
   if (sm_sel > 48 * 1024)
     cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_sel);
-  select_kernel<<<grid, THREADS, sm_sel, s>>>(partial, rp.nsplit, rp.Epad, b_router, sel_bias,
+  select_kernel<<<grid, THREADS, sm_sel, s>>>(partial, nsplit, rp.Epad, b_router, sel_bias,
                                               logits, topk_idx, topk_w, p);
   return cudaGetLastError();
 }
