@@ -32,7 +32,9 @@ struct Cfg {
 struct RouterPlan {
   int Epad, dpad, kb_per_split, nsplit;
   int n_acc, acc_cols;   // TMEM accumulators per CTA and columns per accumulator
-  size_t ws_bytes;       // bf16 3-term split of the router weight [Epad, 3*dpad]
+  int stacked_n;         // 1: the three terms stacked along N (3*Epad <= 256), x read once;
+                         // 0: stacked along K, x read once per term
+  size_t ws_bytes;       // bf16 3-term split of the router weight (3 * Epad * dpad)
   size_t partial_bytes;  // fp32 partial logits [nsplit, N, Epad]
 };
 constexpr int kSmTarget = 148;  // SM count the router slicing is planned for

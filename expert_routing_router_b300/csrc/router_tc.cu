@@ -7,11 +7,14 @@
 // into three bf16 terms W = W0 + W1 + W2 (W0 = bf16(W), W1 = bf16(W - W0),
 // W2 = bf16(W - W0 - W1); both differences are exact in fp32), every product
 // x * Ws is exact in the fp32 accumulator, and what is left out is about 2^-27 |W|.
-// The three terms are stacked along K, so one GEMM with K' = 3 * dpad computes
-//   logits = x . W0^T + x . W1^T + x . W2^T
-// with the A (x) K-coordinate wrapping modulo dpad.
+// When 3 * Epad fits one MMA's N (<= 256, i.e. up to 64 experts) the three terms are
+// stacked along N: Ws is [3*Epad, dpad] and each K block of x meets all three terms
+// in one MMA, into three column ranges of the accumulator that the epilogue adds; x is
+// read once.  Otherwise they are stacked along K: Ws is [Epad, 3*dpad], one GEMM with
+// K' = 3 * dpad computes x . W0^T + x . W1^T + x . W2^T with the x K-coordinate
+// wrapping modulo dpad (x read three times).
 //
-//   split_kernel   W [E, d] fp32 -> Ws [Epad, 3*dpad] bf16 (zero padded)
+//   split_kernel   W [E, d] fp32 -> Ws (either layout) bf16 (zero padded)
 //   router_gemm    one CTA per (128-token tile, K' slice): TMA -> 4-stage ring ->
 //                  tcgen05.mma (M=128, N=Epad) -> TMEM -> fp32 partial logits
 // Slices ("split-K") put all SMs to work when there are few token tiles; the
@@ -53,7 +56,8 @@ struct RParams {
   float* partial;  // [nsplit][N][Epad]
   int* err;
   int N, Epad, nkb_d, kb_per_split, total_kb, n_acc, acc_cols;
-  uint32_t idesc, tmem_cols;
+  int terms_n;  // term column ranges per accumulator (3 when stacked along N, else 1)
+  uint32_t idesc, tmem_cols, b_bytes;
 };
 
 __device__ bool wait_bar(uint64_t* b, uint32_t parity, RCtl* ctl, int* err, int code) {
@@ -73,7 +77,7 @@ __device__ bool wait_bar(uint64_t* b, uint32_t parity, RCtl* ctl, int* err, int 
 }
 
 __global__ void split_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ Ws, int E,
-                             int d, int Epad, int dpad) {
+                             int d, int Epad, int dpad, int stacked_n) {
   const int64_t total = (int64_t)Epad * dpad;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -83,10 +87,16 @@ __global__ void split_kernel(const float* __restrict__ W, __nv_bfloat16* __restr
     const float r1 = w - __bfloat162float(w0);
     const __nv_bfloat16 w1 = __float2bfloat16_rn(r1);
     const float r2 = r1 - __bfloat162float(w1);
-    __nv_bfloat16* row = Ws + (int64_t)e * 3 * dpad;
-    row[c] = w0;
-    row[dpad + c] = w1;
-    row[2 * dpad + c] = __float2bfloat16_rn(r2);
+    if (stacked_n) {  // term t of expert e is row t * Epad + e of [3*Epad, dpad]
+      Ws[(int64_t)e * dpad + c] = w0;
+      Ws[((int64_t)Epad + e) * dpad + c] = w1;
+      Ws[((int64_t)2 * Epad + e) * dpad + c] = __float2bfloat16_rn(r2);
+    } else {          // term t at columns t * dpad of row e of [Epad, 3*dpad]
+      __nv_bfloat16* row = Ws + (int64_t)e * 3 * dpad;
+      row[c] = w0;
+      row[dpad + c] = w1;
+      row[2 * dpad + c] = __float2bfloat16_rn(r2);
+    }
   }
 }
 
@@ -101,7 +111,7 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
   const int m0 = blockIdx.x * BM;
   const int kb0 = blockIdx.y * p.kb_per_split;
   const int kb1 = min(kb0 + p.kb_per_split, p.total_kb);
-  const uint32_t b_bytes = (uint32_t)p.Epad * BK * 2;
+  const uint32_t b_bytes = p.b_bytes;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -196,13 +206,16 @@ router_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constan
         uint32_t v[32];
         tmem_ld32(lane_base + (uint32_t)c, v);
         tmem_ld_wait(v);
-        for (int a = 1; a < n_used; ++a) {  // fixed-order round-to-nearest sum
-          uint32_t u[32];
-          tmem_ld32(lane_base + (uint32_t)(a * p.acc_cols + c), u);
-          tmem_ld_wait(u);
+        // fixed-order round-to-nearest sum over the term ranges, then the accumulators
+        for (int tm = 0; tm < p.terms_n; ++tm) {
+          for (int a = (tm == 0 ? 1 : 0); a < n_used; ++a) {
+            uint32_t u[32];
+            tmem_ld32(lane_base + (uint32_t)(a * p.acc_cols + tm * p.Epad + c), u);
+            tmem_ld_wait(u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            v[i] = __float_as_uint(__fadd_rn(__uint_as_float(v[i]), __uint_as_float(u[i])));
+            for (int i = 0; i < 32; ++i)
+              v[i] = __float_as_uint(__fadd_rn(__uint_as_float(v[i]), __uint_as_float(u[i])));
+          }
         }
         if (row < p.N) {
 #pragma unroll
@@ -253,12 +266,14 @@ RouterPlan router_plan(const Cfg& c) {
   RouterPlan rp;
   rp.Epad = (c.E + 31) / 32 * 32;
   rp.dpad = (c.d + BK - 1) / BK * BK;
+  rp.stacked_n = 3 * rp.Epad <= 256 ? 1 : 0;
+  const int ncols = rp.stacked_n ? 3 * rp.Epad : rp.Epad;  // MMA N
   rp.acc_cols = 32;
-  while (rp.acc_cols < rp.Epad) rp.acc_cols <<= 1;
+  while (rp.acc_cols < ncols) rp.acc_cols <<= 1;
   rp.n_acc = 512 / rp.acc_cols;
   if (rp.n_acc > 4) rp.n_acc = 4;
   const int tiles = (c.N + BM - 1) / BM;
-  const int total_kb = 3 * (rp.dpad / BK);
+  const int total_kb = (rp.stacked_n ? 1 : 3) * (rp.dpad / BK);
   int ns = kSmTarget / tiles;                   // fill the GPU when tiles are few
   if (ns > 16) ns = 16;
   const int chains = (total_kb * BK + kChainK - 1) / kChainK;
@@ -280,11 +295,12 @@ cudaError_t launch_router_gemm(const Cfg& c, const RouterPlan& rp, const void* x
   const int64_t n_el = (int64_t)rp.Epad * rp.dpad;
   int sgrid = (int)((n_el + 255) / 256);
   if (sgrid > num_sms() * 8) sgrid = num_sms() * 8;
-  split_kernel<<<sgrid, 256, 0, s>>>(w_router, Ws, c.E, c.d, rp.Epad, rp.dpad);
+  split_kernel<<<sgrid, 256, 0, s>>>(w_router, Ws, c.E, c.d, rp.Epad, rp.dpad, rp.stacked_n);
   CUtensorMap mx, mw;
-  if (!make_map(&mx, x, c.d, c.N, BM) ||
-      !make_map(&mw, Ws, (uint64_t)3 * rp.dpad, rp.Epad, (uint32_t)rp.Epad))
-    return cudaErrorInvalidValue;
+  const bool ok = rp.stacked_n
+                      ? make_map(&mw, Ws, (uint64_t)rp.dpad, 3 * rp.Epad, (uint32_t)(3 * rp.Epad))
+                      : make_map(&mw, Ws, (uint64_t)3 * rp.dpad, rp.Epad, (uint32_t)rp.Epad);
+  if (!ok || !make_map(&mx, x, c.d, c.N, BM)) return cudaErrorInvalidValue;
   RParams p;
   p.partial = partial;
   p.err = status;
@@ -292,8 +308,11 @@ cudaError_t launch_router_gemm(const Cfg& c, const RouterPlan& rp, const void* x
   p.Epad = rp.Epad;
   p.nkb_d = rp.dpad / BK;
   p.kb_per_split = rp.kb_per_split;
-  p.total_kb = 3 * p.nkb_d;
-  p.idesc = idesc_bf16_f32(BM, rp.Epad);
+  p.total_kb = (rp.stacked_n ? 1 : 3) * p.nkb_d;
+  p.terms_n = rp.stacked_n ? 3 : 1;
+  const int ncols = rp.stacked_n ? 3 * rp.Epad : rp.Epad;
+  p.idesc = idesc_bf16_f32(BM, ncols);
+  p.b_bytes = (uint32_t)ncols * BK * 2;
   p.n_acc = rp.n_acc;
   p.acc_cols = rp.acc_cols;
   uint32_t cols = 32;
