@@ -78,15 +78,18 @@ struct Ctl {
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctl);
 
 // Bounded wait.  False when the wait expired (error recorded) or another role
-// already gave up.
-__device__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl, int* err, int code) {
+// already gave up.  Waits on another role's progress (ring slot freed, accumulator
+// filled or drained) get twice the limit of the MMA issuer's wait for a loaded slot,
+// so a copy that never lands is reported as such (code 3), not as a stalled consumer.
+__device__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl, int* err, int code,
+                          uint64_t limit_ns = 2 * WAIT_NS) {
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = now_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(b, parity)) return true;
     if ((i & 63) == 0) {
       if (*(volatile int*)&ctl->abort) return false;
-      if (now_ns() - t0 > WAIT_NS) {
+      if (now_ns() - t0 > limit_ns) {
         *(volatile int*)&ctl->abort = 1;
         atomicExch(err, code);
         return false;
@@ -285,7 +288,7 @@ grouped_ffn_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_consta
         tc_fence_after();
         const uint32_t dt = tmem_base + (uint32_t)(acc * BN);
         for (int k0 = 0; k0 < K; k0 += BK) {
-          if (!mbar_wait(&ctl->full[stage], phase, ctl, p.err, 3)) {
+          if (!mbar_wait(&ctl->full[stage], phase, ctl, p.err, 3, WAIT_NS)) {
             ok = false;
             break;
           }

@@ -408,6 +408,12 @@ EDGE = {
                                           num_ranks=3, score_fn=0, num_groups=1, topk_groups=1,
                                           capacity_factor=1.1, d_ff=392, shared_d_ff=0,
                                           sel_bias_std=0.0),
+    # skewed expert sizes (66, 15, 212, 267 rows) on the 128-row-tile kernels: last
+    # tiles of 11 to 84 rows, an expert of one partial tile, a 560-row shared expert
+    "skewed_segments_ragged_tails": small(tokens=560, hidden=200, num_experts=4, top_k=1,
+                                               num_ranks=2, score_fn=0, num_groups=1,
+                                               topk_groups=1, router_offset_std=0.6,
+                                               d_ff=136, shared_d_ff=264, sel_bias_std=0.0),
     "capacity_exact_boundary": small(tokens=256, hidden=64, num_experts=4, top_k=1, num_ranks=4,
                                      score_fn=0, num_groups=1, topk_groups=1,
                                      capacity_factor=1.0, d_ff=32, shared_d_ff=0,
