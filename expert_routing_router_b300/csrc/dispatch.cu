@@ -190,11 +190,26 @@ constexpr int UNROLL = 4;
 __global__ void __launch_bounds__(TP)
 permute_kernel(const uint4* __restrict__ x, uint4* __restrict__ xperm,
                const int32_t* __restrict__ slot_of, int N, int k, int nvec) {
-  for (int t = blockIdx.x; t < N; t += gridDim.x) {
-    int slots[kMaxTopK];
+  // a token's slots are loaded one token ahead, so the row copy does not wait on them;
+  // a token whose every choice was dropped is not read at all
+  int slots[kMaxTopK];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) slots[j] = (j < k) ? slot_of[(int64_t)t * k + j] : -1;
+  for (int j = 0; j < kMaxTopK; ++j)
+    slots[j] = (j < k && blockIdx.x < N) ? slot_of[(int64_t)blockIdx.x * k + j] : -1;
+  for (int t = blockIdx.x; t < N; t += gridDim.x) {
+    const int tn = t + gridDim.x;
+    int next[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) next[j] = (j < k && tn < N) ? slot_of[(int64_t)tn * k + j] : -1;
+    bool any = false;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) any |= slots[j] >= 0;
     const uint4* src = x + (int64_t)t * nvec;
+    if (!any) {
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) slots[j] = next[j];
+      continue;
+    }
     for (int v0 = threadIdx.x; v0 < nvec; v0 += TP * UNROLL) {
       uint4 buf[UNROLL];
 #pragma unroll
@@ -212,6 +227,8 @@ permute_kernel(const uint4* __restrict__ x, uint4* __restrict__ xperm,
         }
       }
     }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) slots[j] = next[j];
   }
 }
 

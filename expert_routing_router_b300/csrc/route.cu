@@ -70,9 +70,9 @@ struct RouteParams {
 };
 
 // Selection for the tokens of one tile whose logits sit in shared memory
-// (lt[r * EP + e] for r < TM), one warp per token: score, optional group limit, k
+// (lt[r * EP + e] for r < rows_tile), one warp per token: score, optional group limit, k
 // rounds of warp-shuffle arg-max, combine weights.  All threads of the CTA call it.
-__device__ void select_tile(float* lt, int EP, int t0, const RouteParams& p,
+__device__ void select_tile(float* lt, int EP, int t0, int rows_tile, const RouteParams& p,
                             const float* __restrict__ sel_bias, int32_t* __restrict__ topk_idx,
                             float* __restrict__ topk_w) {
   const int E = p.E;
@@ -80,7 +80,7 @@ __device__ void select_tile(float* lt, int EP, int t0, const RouteParams& p,
   const int warp = threadIdx.x >> 5;
   const int EJ = (E + 31) / 32;
   const int gs = E / p.G;
-  for (int r = warp; r < TM; r += THREADS / 32) {
+  for (int r = warp; r < rows_tile; r += THREADS / 32) {
     const int t = t0 + r;
     if (t >= p.N) break;
     float* row = lt + r * EP;
@@ -264,32 +264,50 @@ route_kernel(const T* __restrict__ x, const float* __restrict__ W, const float* 
   }
   __syncthreads();  // rows are overwritten with ranking keys below
 
-  select_tile(lt, EP, t0, p, sel_bias, topk_idx, topk_w);
+  select_tile(lt, EP, t0, TM, p, sel_bias, topk_idx, topk_w);
 }
 
 // Router logits from the tensor-core path: fixed-order sum of the K slices plus the
-// router bias, written out, then the same selection as the SIMT path.
-__global__ void __launch_bounds__(THREADS)
+// router bias, written out, then the same selection as the SIMT path.  TS tokens per
+// CTA: 32, or 8 for small batches, whose few token tiles the GEMM splits into many K
+// slices (more CTAs share the slice sums).
+template <int TS>
+__global__ void __launch_bounds__(THREADS, 4)
 select_kernel(const float* __restrict__ partial, int nsplit, int Epad, const float* __restrict__ b,
               const float* __restrict__ sel_bias, float* __restrict__ logits,
               int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteParams p) {
   extern __shared__ float smem[];
   const int E = p.E, EP = E + 1;
   float* lt = smem;
-  const int t0 = blockIdx.x * TM;
-  for (int q = threadIdx.x; q < TM * E; q += THREADS) {
-    const int r = q / E, e = q % E;
-    const int t = t0 + r;
-    if (t < p.N) {
-      float v = partial[(int64_t)t * Epad + e];
-      for (int sp = 1; sp < nsplit; ++sp) v += partial[((int64_t)sp * p.N + t) * Epad + e];
-      v += b ? b[e] : 0.0f;
-      lt[r * EP + e] = v;
-      logits[(int64_t)t * E + e] = v;
+  const int t0 = blockIdx.x * TS;
+  const int rows = min(TS, p.N - t0);
+  // Thread c (< E <= THREADS) owns column c of the tile and adds the K slices into it
+  // slice by slice: its TS loads of one slice are independent, so a slice costs about
+  // one memory latency; the additions run in slice order 0, 1, ..., nsplit-1.
+  static_assert(kMaxExperts <= THREADS, "one thread per expert column");
+  const int col = threadIdx.x;
+  if (col < E) {
+    const float bc = b ? b[col] : 0.0f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float* ps = partial + ((int64_t)sp * p.N + t0) * Epad + col;
+      float v[TS];
+#pragma unroll
+      for (int r = 0; r < TS; ++r) v[r] = r < rows ? ps[(int64_t)r * Epad] : 0.0f;
+#pragma unroll
+      for (int r = 0; r < TS; ++r)
+        if (r < rows) lt[r * EP + col] = sp == 0 ? v[r] : lt[r * EP + col] + v[r];
+    }
+#pragma unroll
+    for (int r = 0; r < TS; ++r) {
+      if (r < rows) {
+        const float o = lt[r * EP + col] + bc;
+        lt[r * EP + col] = o;
+        logits[(int64_t)(t0 + r) * E + col] = o;
+      }
     }
   }
   __syncthreads();
-  select_tile(lt, EP, t0, p, sel_bias, topk_idx, topk_w);
+  select_tile(lt, EP, t0, rows, p, sel_bias, topk_idx, topk_w);
 }
 
 }  // namespace
@@ -301,6 +319,8 @@ select_kernel(const float* __restrict__ partial, int nsplit, int Epad, const flo
 // select_kernel adds the bias and selects.  The weight is read once and nothing is
 // re-split per call (the tensor-core path rewrites the 3-term bf16 split every call).
 constexpr int kSmallRouteTokens = 16;
+// Batches up to this many tokens select with 8-token tiles (see select_kernel).
+constexpr int kSmallSelectTokens = 4096;
 
 __global__ void __launch_bounds__(THREADS)
 route_small_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
@@ -372,10 +392,18 @@ cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, con
     cudaError_t e = launch_router_gemm(c, rp, x, w_router, ws_split, partial, status, s);
     if (e != cudaSuccess) return e;
   }
-  if (sm_sel > 48 * 1024)
-    cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_sel);
-  select_kernel<<<grid, THREADS, sm_sel, s>>>(partial, nsplit, rp.Epad, b_router, sel_bias,
-                                              logits, topk_idx, topk_w, p);
+  if (c.N <= kSmallSelectTokens) {
+    constexpr int TS = 8;
+    const size_t sm = (size_t)TS * (c.E + 1) * sizeof(float);
+    select_kernel<TS><<<(c.N + TS - 1) / TS, THREADS, sm, s>>>(
+        partial, nsplit, rp.Epad, b_router, sel_bias, logits, topk_idx, topk_w, p);
+  } else {
+    if (sm_sel > 48 * 1024)
+      cudaFuncSetAttribute(select_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sm_sel);
+    select_kernel<TM><<<grid, THREADS, sm_sel, s>>>(partial, nsplit, rp.Epad, b_router, sel_bias,
+                                                    logits, topk_idx, topk_w, p);
+  }
   return cudaGetLastError();
 }
 
