@@ -106,6 +106,79 @@ combine_kernel(const uint4* __restrict__ yperm, const int32_t* __restrict__ slot
   }
 }
 
+// top-1 / top-2 layers with short rows (nvec <= TC): TC / nvec tokens per CTA pass, one
+// 16-byte vector per thread, and each token's two slots and weights loaded one pass
+// ahead, so the row loads of a pass wait on no index load.  Same sum order as above.
+template <typename T>
+__global__ void __launch_bounds__(TC)
+combine_k2_kernel(const uint4* __restrict__ yperm, const int32_t* __restrict__ slot_of,
+                  const float* __restrict__ topk_w, const uint4* __restrict__ residual,
+                  const uint4* __restrict__ yshared, uint4* __restrict__ out, int N, int k,
+                  int nvec) {
+  constexpr int L = Vec<T>::n;
+  const int tpp = TC / nvec;              // tokens per pass
+  const int sub = threadIdx.x / nvec;     // this thread's token within the pass
+  const int v = threadIdx.x - sub * nvec;
+  if (sub >= tpp) return;
+  const int step = gridDim.x * tpp;
+  int t = blockIdx.x * tpp + sub;
+  int s0 = -1, s1 = -1;
+  float w0 = 0.0f, w1 = 0.0f;
+  if (t < N) {
+    s0 = slot_of[(int64_t)t * k];
+    w0 = topk_w[(int64_t)t * k];
+    if (k > 1) {
+      s1 = slot_of[(int64_t)t * k + 1];
+      w1 = topk_w[(int64_t)t * k + 1];
+    }
+  }
+  for (; t < N; t += step) {
+    const int tn = t + step;
+    int n0 = -1, n1 = -1;
+    float nw0 = 0.0f, nw1 = 0.0f;
+    if (tn < N) {
+      n0 = slot_of[(int64_t)tn * k];
+      nw0 = topk_w[(int64_t)tn * k];
+      if (k > 1) {
+        n1 = slot_of[(int64_t)tn * k + 1];
+        nw1 = topk_w[(int64_t)tn * k + 1];
+      }
+    }
+    uint4 r0 = make_uint4(0, 0, 0, 0), r1 = r0, rres = r0, rsh = r0;
+    if (s0 >= 0) r0 = ld_stream_u4(yperm + (int64_t)s0 * nvec + v);
+    if (s1 >= 0) r1 = ld_stream_u4(yperm + (int64_t)s1 * nvec + v);
+    if (residual) rres = ld_stream_u4(residual + (int64_t)t * nvec + v);
+    if (yshared) rsh = ld_stream_u4(yshared + (int64_t)t * nvec + v);
+    float acc[L], tmp[L];
+    if (residual) {
+      Vec<T>::load(&rres, acc);
+    } else {
+#pragma unroll
+      for (int i = 0; i < L; ++i) acc[i] = 0.0f;
+    }
+    if (yshared) {
+      Vec<T>::load(&rsh, tmp);
+#pragma unroll
+      for (int i = 0; i < L; ++i) acc[i] += tmp[i];
+    }
+    if (s0 >= 0) {
+      Vec<T>::load(&r0, tmp);
+#pragma unroll
+      for (int i = 0; i < L; ++i) acc[i] = fmaf(w0, tmp[i], acc[i]);
+    }
+    if (s1 >= 0) {
+      Vec<T>::load(&r1, tmp);
+#pragma unroll
+      for (int i = 0; i < L; ++i) acc[i] = fmaf(w1, tmp[i], acc[i]);
+    }
+    Vec<T>::store(out + (int64_t)t * nvec + v, acc);
+    s0 = n0;
+    s1 = n1;
+    w0 = nw0;
+    w1 = nw1;
+  }
+}
+
 __global__ void bias_update_kernel(const int32_t* __restrict__ counts, float* __restrict__ bias,
                                    int E, int64_t mean_num, float step) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -130,11 +203,21 @@ cudaError_t launch_combine(const Cfg& c, const void* yperm, const int32_t* slot_
   const uint4* rs = static_cast<const uint4*>(residual);
   const uint4* ys = static_cast<const uint4*>(yshared);
   uint4* o = static_cast<uint4*>(out);
-  if (c.act == MOE_DTYPE_F32)
+  if (c.k <= 2 && nvec <= TC) {
+    const int tpp = TC / nvec;
+    int g2 = num_sms() * 8;
+    if ((int64_t)g2 * tpp > c.N) g2 = (c.N + tpp - 1) / tpp;
+    if (c.act == MOE_DTYPE_F32)
+      combine_k2_kernel<float><<<g2, TC, 0, s>>>(yp, slot_of, topk_w, rs, ys, o, c.N, c.k, nvec);
+    else
+      combine_k2_kernel<__nv_bfloat16><<<g2, TC, 0, s>>>(yp, slot_of, topk_w, rs, ys, o, c.N,
+                                                         c.k, nvec);
+  } else if (c.act == MOE_DTYPE_F32) {
     combine_kernel<float><<<grid, TC, 0, s>>>(yp, slot_of, topk_w, rs, ys, o, c.N, c.k, nvec);
-  else
+  } else {
     combine_kernel<__nv_bfloat16><<<grid, TC, 0, s>>>(yp, slot_of, topk_w, rs, ys, o, c.N, c.k,
                                                        nvec);
+  }
   return cudaGetLastError();
 }
 
