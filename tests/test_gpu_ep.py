@@ -1,0 +1,107 @@
+"""Expert-parallel layer on one GPU: every rank's route, dispatch, local experts,
+shared expert and combine run through the C ABI, the exchanges as copies between the
+ranks' buffers (ranks one after another; no rank waits on another).  Each rank's
+layer is checked against the oracle step by step, exactly as a single-device layer
+on that rank's tokens, with the expert FFN rows computed on the rank that owns the
+expert and brought back by the return exchange.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from expert_routing_router_b300 import ep, workloads as W
+from test_gpu_parity import check_layer, host, host_weights, small
+
+pytestmark = pytest.mark.gpu
+
+
+def _ranks(w, R, seed=0):
+    """R ranks of the layer: the same weights, each its own slice of the tokens."""
+    whole = W.make_inputs(dataclasses.replace(w, tokens=w.tokens * R), seed=seed, device="cuda")
+    ranks = []
+    for r in range(R):
+        inp = dict(whole)
+        inp["x"] = whole["x"][r * w.tokens:(r + 1) * w.tokens].contiguous()
+        ranks.append(ep.RankLayer(w, r, inp))
+    return ranks, whole
+
+
+EP_CASES = {
+    # 2 ranks, contiguous experts, sigmoid + groups, shared expert, no capacity
+    "two_ranks_contiguous_shared": (small(tokens=600, hidden=264, num_experts=16, top_k=4,
+                                          num_ranks=2, d_ff=200, shared_d_ff=72), 2),
+    # 4 ranks, round-robin experts, softmax, capacity with drops
+    "four_ranks_round_robin_capacity": (small(tokens=300, hidden=136, num_experts=10, top_k=3,
+                                              num_ranks=4, rank_map=1, score_fn=0,
+                                              num_groups=1, topk_groups=1, capacity_factor=1.0,
+                                              d_ff=96, shared_d_ff=0, sel_bias_std=0.0), 4),
+    # DeepSeek-V3-shaped experts on 2 ranks (128 local experts each), fewer tokens
+    "dsv3_shape_two_ranks": (dataclasses.replace(W.DSV3_PREFILL, name="dsv3_ep", tokens=1024,
+                                                 num_ranks=2), 2),
+}
+
+
+@pytest.mark.parametrize("name", list(EP_CASES))
+def test_expert_parallel_layer_loopback(name):
+    w, R = EP_CASES[name]
+    ranks, whole = _ranks(w, R)
+    sb0 = None if whole["sel_bias"] is None else whole["sel_bias"].clone()
+    plans = ep.run_layer_loopback(ranks, bias_step=w.bias_step)
+    torch.cuda.synchronize()
+    hw = host_weights(whole)
+    total = 0
+    for r, (rank, plan) in enumerate(zip(ranks, plans)):
+        assert int(rank.b.workspace[:4].view(torch.int32).item()) == 0
+        assert int(rank.local_ws[:4].view(torch.int32).item()) == 0
+        # the plan's send chunks are this rank's dispatch segments
+        st = host(rank.b.expert_start)
+        for (dst, e, off, n) in plan.send_chunks:
+            assert off == st[e]
+        total += plan.recv_rows
+        if sb0 is not None:  # check this rank's layer with the bias it routed with
+            rank.inp = dict(rank.inp, sel_bias=sb0)
+        n_tok = None if w.tokens <= 1024 and w.hidden <= 1024 else 96
+        check_layer(w, rank.inp, rank.b, n_sample_tokens=n_tok,
+                    n_sample_rows=None if n_tok is None else 256, seed=r, hw=hw)
+    assert total == sum(int(rk.b.num_kept.item()) for rk in ranks)
+    if sb0 is not None and w.bias_step:
+        # sign rule on the counts summed over the ranks (all ranks' tokens)
+        counts = sum(host(rk.b.expert_counts).astype(np.int64) for rk in ranks)
+        mean_num = w.tokens * R * w.top_k
+        sgn = np.sign(counts * w.num_experts - mean_num)
+        ref = (host(sb0) - np.float32(w.bias_step) * sgn.astype(np.float32)).astype(np.float32)
+        np.testing.assert_array_equal(host(whole["sel_bias"]), ref)
+
+
+def test_expert_parallel_layer_dist_single_rank():
+    """run_layer_dist through an NCCL process group of one rank: the all-gather of the
+    kept counts, the plan, both exchanges (all chunks are this rank's own), the local
+    experts, the shared expert, the combine and the all-reduced bias update."""
+    import os
+    import socket
+    import torch.distributed as dist
+    w, _ = EP_CASES["two_ranks_contiguous_shared"]
+    w = dataclasses.replace(w, num_ranks=1)
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                            world_size=1)
+    try:
+        ranks, whole = _ranks(w, 1, seed=4)
+        sb0 = whole["sel_bias"].clone()
+        plan = ep.run_layer_dist(ranks[0], bias_step=w.bias_step)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    r = ranks[0]
+    assert plan.recv_rows == int(r.b.num_kept.item())
+    assert int(r.local_ws[:4].view(torch.int32).item()) == 0
+    check_layer(w, dict(r.inp, sel_bias=sb0), r.b)
+    counts = host(r.b.expert_counts).astype(np.int64)
+    sgn = np.sign(counts * w.num_experts - w.tokens * w.top_k)
+    ref = (host(sb0) - np.float32(w.bias_step) * sgn.astype(np.float32)).astype(np.float32)
+    np.testing.assert_array_equal(host(whole["sel_bias"]), ref)
