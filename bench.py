@@ -199,7 +199,7 @@ def oracle_step(oracle, w, h, n):
 def oracle_sample_size(oracle, w, h, budget_s):
     """Largest token sample whose oracle pass fits in about budget_s seconds (the
     oracle runs tokens in parallel, so calibrate with one token per host thread)."""
-    n = max(2, min(w.tokens, oracle.num_threads()))
+    n = min(w.tokens, max(2, oracle.num_threads()))
     t0 = time.perf_counter()
     oracle_step(oracle, w, h, n)
     per_tok = (time.perf_counter() - t0) / n

@@ -71,6 +71,15 @@ def _act(a):
     raise TypeError(f"activation arrays must be float32 or uint16 (bf16 bits), got {a.dtype}")
 
 
+def _tokens(tokens, N):
+    """Token indices as int32, every one a row of the N-token batch (the C side reads
+    row t of x, slot_of and the weights without a bounds check)."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+    if tokens.size and (tokens.min() < 0 or tokens.max() >= N):
+        raise ValueError(f"token index outside the batch of {N} tokens")
+    return tokens
+
+
 def num_threads():
     return _lib().oracle_num_threads()
 
@@ -175,7 +184,7 @@ def combine(tokens, x, yperm, slot_of, w, ys=None):
     if ys is not None:
         ys, c3 = _act(ys)
         assert c3 == code
-    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    tokens = _tokens(tokens, N)
     out = np.empty((tokens.size, d), dtype=np.float64)
     _lib().oracle_combine(tokens.size, _p(tokens), d, k, code, _p(x), _p(yperm), _p(ys),
                           _p(slot_of), _p(w), _p(out))
@@ -201,7 +210,7 @@ def layer_tokens(tokens, x, idx, w, slot_of, w_gate_up, w_down, shared_gate_up=N
         sgu, _ = _act(shared_gate_up)
         sd, _ = _act(shared_down)
         Fs = sgu.shape[0] // 2
-    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    tokens = _tokens(tokens, N)
     out = np.empty((tokens.size, d), dtype=np.float64)
     _lib().oracle_layer_tokens(tokens.size, _p(tokens), d, E, k, F, Fs, code, _p(x), _p(idx),
                                _p(w), _p(slot_of), _p(wgu), _p(wd), _p(sgu), _p(sd), _p(out))
@@ -250,7 +259,7 @@ def combine_q8(tokens, x, yq, yscale, slot_of, w, ys=None):
     if ys is not None:
         ys, c3 = _act(ys)
         assert c3 == code
-    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    tokens = _tokens(tokens, N)
     out = np.empty((tokens.size, d), dtype=np.float64)
     _lib().oracle_combine_q8(tokens.size, _p(tokens), d, k, code, _p(x), _p(yq), _p(yscale),
                              _p(ys), _p(slot_of), _p(w), _p(out))
@@ -363,7 +372,7 @@ def dispatch_backward(tokens, dout, dxperm, slot_of, dxs=None, dxr=None):
         dxs, c2 = _act(dxs)
         assert c2 == code
     dxr = None if dxr is None else np.ascontiguousarray(dxr, dtype=np.float32)
-    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    tokens = _tokens(tokens, N)
     out = np.empty((tokens.size, d), np.float64)
     _lib().oracle_dispatch_backward(tokens.size, _p(tokens), d, k, code, _p(dout), _p(dxs),
                                     _p(dxr), _p(dxperm), _p(slot_of), _p(out))
