@@ -281,28 +281,38 @@ select_kernel(const float* __restrict__ partial, int nsplit, int Epad, const flo
   float* lt = smem;
   const int t0 = blockIdx.x * TS;
   const int rows = min(TS, p.N - t0);
-  // Thread c (< E <= THREADS) owns column c of the tile and adds the K slices into it
-  // slice by slice: its TS loads of one slice are independent, so a slice costs about
-  // one memory latency; the additions run in slice order 0, 1, ..., nsplit-1.
-  static_assert(kMaxExperts <= THREADS, "one thread per expert column");
-  const int col = threadIdx.x;
-  if (col < E) {
-    const float bc = b ? b[col] : 0.0f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float* ps = partial + ((int64_t)sp * p.N + t0) * Epad + col;
-      float v[TS];
-#pragma unroll
-      for (int r = 0; r < TS; ++r) v[r] = r < rows ? ps[(int64_t)r * Epad] : 0.0f;
-#pragma unroll
-      for (int r = 0; r < TS; ++r)
-        if (r < rows) lt[r * EP + col] = sp == 0 ? v[r] : lt[r * EP + col] + v[r];
+  if (nsplit == 1) {
+    // one slice: each thread moves whole elements (bias added, written out)
+    for (int q = threadIdx.x; q < rows * E; q += THREADS) {
+      const int r = q / E, e = q - r * E;
+      const float o = __ldg(partial + (int64_t)(t0 + r) * Epad + e) + (b ? b[e] : 0.0f);
+      lt[r * EP + e] = o;
+      logits[(int64_t)(t0 + r) * E + e] = o;
     }
+  } else {
+    // Thread c (< E <= THREADS) owns column c of the tile and adds the K slices into
+    // it slice by slice: its TS loads of one slice are independent, so a slice costs
+    // about one memory latency; the additions run in slice order 0, 1, ..., nsplit-1.
+    static_assert(kMaxExperts <= THREADS, "one thread per expert column");
+    const int col = threadIdx.x;
+    if (col < E) {
+      const float bc = b ? b[col] : 0.0f;
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float* ps = partial + ((int64_t)sp * p.N + t0) * Epad + col;
+        float v[TS];
 #pragma unroll
-    for (int r = 0; r < TS; ++r) {
-      if (r < rows) {
-        const float o = lt[r * EP + col] + bc;
-        lt[r * EP + col] = o;
-        logits[(int64_t)(t0 + r) * E + col] = o;
+        for (int r = 0; r < TS; ++r) v[r] = r < rows ? __ldg(ps + (int64_t)r * Epad) : 0.0f;
+#pragma unroll
+        for (int r = 0; r < TS; ++r)
+          if (r < rows) lt[r * EP + col] = sp == 0 ? v[r] : lt[r * EP + col] + v[r];
+      }
+#pragma unroll
+      for (int r = 0; r < TS; ++r) {
+        if (r < rows) {
+          const float o = lt[r * EP + col] + bc;
+          lt[r * EP + col] = o;
+          logits[(int64_t)(t0 + r) * E + col] = o;
+        }
       }
     }
   }
