@@ -37,6 +37,15 @@ EP_CASES = {
                                               num_ranks=4, rank_map=1, score_fn=0,
                                               num_groups=1, topk_groups=1, capacity_factor=1.0,
                                               d_ff=96, shared_d_ff=0, sel_bias_std=0.0), 4),
+    # few rows per expert: the token-major small-segment kernels (local experts and the
+    # shared-expert call with no routed rows)
+    "decode_sized_two_ranks": (small(tokens=40, hidden=264, num_experts=64, top_k=4,
+                                     num_ranks=2, num_groups=8, topk_groups=4, d_ff=200,
+                                     shared_d_ff=72), 2),
+    # many rows per expert: the SM-pair kernels on both sides
+    "pair_kernel_two_ranks": (small(tokens=1500, hidden=264, num_experts=4, top_k=2,
+                                    num_ranks=2, num_groups=2, topk_groups=1, d_ff=200,
+                                    shared_d_ff=72), 2),
     # DeepSeek-V3-shaped experts on 2 ranks (128 local experts each), fewer tokens
     "dsv3_shape_two_ranks": (dataclasses.replace(W.DSV3_PREFILL, name="dsv3_ep", tokens=1024,
                                                  num_ranks=2), 2),
