@@ -154,9 +154,10 @@ def exchange_loopback(plans, send_bufs, recv_bufs, reverse=False):
 class RankLayer:
     """One rank of an expert-parallel layer: its LayerBuffers (the workload's
     num_ranks is the number of ranks), its local experts' weights, and the receive
-    buffers sized for the worst case (every rank sends every row here)."""
+    buffers: recv_capacity rows, by default the worst case (every rank sends every row
+    here, R * tokens * top_k); a step whose plan needs more raises before any copy."""
 
-    def __init__(self, w, rank, inp, device="cuda"):
+    def __init__(self, w, rank, inp, device="cuda", recv_capacity=None):
         if w.rank_map != RANK_ROUND_ROBIN and w.num_experts % w.num_ranks:
             raise ValueError("contiguous expert blocks need num_experts % num_ranks == 0")
         self.w, self.rank, self.inp = w, rank, inp
@@ -173,7 +174,8 @@ class RankLayer:
             e0, e1 = self.local[0], self.local[-1] + 1
             self.w_gate_up = inp["w_gate_up"][e0:e1]
             self.w_down = inp["w_down"][e0:e1]
-        cap = max(R * N * k, 1)
+        cap = max(R * N * k if recv_capacity is None else int(recv_capacity), 1)
+        self.recv_capacity = cap
         self.recv_x = torch.empty(cap, d, dtype=w.torch_dtype, device=device)
         self.recv_y = torch.empty(cap, d, dtype=w.torch_dtype, device=device)
         self.local_w = replace(w, name=f"{w.name}.experts{rank}", tokens=cap, top_k=1,
@@ -194,6 +196,11 @@ class RankLayer:
         moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
                          b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
                          b.num_kept, b.workspace, stream)
+
+    def check_plan(self, plan):
+        if plan.recv_rows > self.recv_capacity:
+            raise ValueError(f"rank {self.rank} would receive {plan.recv_rows} rows; its "
+                             f"receive buffers hold {self.recv_capacity}")
 
     def local_ffn(self, plan, stream=None):
         """The local experts on the expert-major receive buffer (recv_x -> recv_y)."""
@@ -230,6 +237,8 @@ def run_layer_loopback(ranks, bias_step=0.0):
     kept = torch.stack([r.b.kept_counts for r in ranks]).cpu().numpy()
     w0 = ranks[0].w
     plans = [ExchangePlan(kept, w0.num_experts, R, w0.rank_map, me) for me in range(R)]
+    for r, plan in zip(ranks, plans):
+        r.check_plan(plan)
     exchange_loopback(plans, [r.b.xperm for r in ranks], [r.recv_x for r in ranks])
     for r, plan in zip(ranks, plans):
         r.local_ffn(plan)
@@ -246,15 +255,19 @@ def run_layer_loopback(ranks, bias_step=0.0):
 
 def run_layer_dist(rank_layer, group=None, bias_step=0.0):
     """This rank's part of the expert-parallel layer over torch.distributed (one rank
-    per GPU): route and dispatch, gather the kept counts, exchange, local experts,
-    return exchange, shared expert, combine, and the bias update from the all-reduced
-    counts.  Returns the plan."""
+    per GPU, every rank with the same receive capacity): route and dispatch, gather the
+    kept counts, exchange, local experts, return exchange, shared expert, combine, and
+    the bias update from the all-reduced counts.  Returns the plan."""
     import torch.distributed as dist
     r = rank_layer
     r.route_dispatch()
     kept = gather_kept(r.b.kept_counts, group)
     w = r.w
     plan = ExchangePlan(kept, w.num_experts, w.num_ranks, w.rank_map, r.rank)
+    # every rank holds every rank's counts, so with the same receive capacity on every
+    # rank all ranks take the same decision here and none is left waiting in an exchange
+    for other in range(w.num_ranks):
+        r.check_plan(ExchangePlan(kept, w.num_experts, w.num_ranks, w.rank_map, other))
     exchange_dist(plan, r.b.xperm, r.recv_x, group=group)
     r.local_ffn(plan)
     exchange_dist(plan, r.b.yperm, r.recv_y, reverse=True, group=group)

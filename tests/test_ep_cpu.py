@@ -165,3 +165,20 @@ def test_exchange_gloo_two_ranks(case):
         p.join(timeout=60)
     assert [r[1] for r in res] == ["ok", "ok"], res
     assert all(p.exitcode == 0 for p in procs)
+
+
+def test_receive_capacity_check_is_the_same_on_every_rank():
+    """A plan that would overflow one rank's receive buffers is refused by every rank
+    (each rank checks all ranks' plans against the shared capacity)."""
+    R, E = 2, 8
+    kept = np.zeros((R, E), np.int64)
+    kept[:, 0] = 50                     # both ranks send 50 rows to expert 0 (rank 0)
+    plans = [ep.ExchangePlan(kept, E, R, 0, me) for me in range(R)]
+    assert [p.recv_rows for p in plans] == [100, 0]
+
+    class Stub:                          # RankLayer.check_plan without device buffers
+        recv_capacity, rank = 64, 1
+        check_plan = ep.RankLayer.check_plan
+    with pytest.raises(ValueError, match="would receive 100 rows"):
+        for other in range(R):
+            Stub().check_plan(plans[other])
