@@ -11,9 +11,15 @@
  *   4. combine   -- moe_combine     return outputs to token order, weighted by the
  *                                   router scores, and sum
  * plus the bias-based balancing step of the section "Load balancing and capacity"
- * (moe_bias_update).  Expert-parallel ranks are logical only: the expert -> rank
- * map yields the per-rank counts and offsets an all-to-all would use as its splits;
- * nothing leaves the GPU.
+ * (moe_bias_update).  Expert-parallel ranks are logical to these calls: the expert
+ * -> rank map yields the per-rank counts and offsets an all-to-all would use as its
+ * splits, and nothing leaves the GPU.  Ranks on separate devices exchange, between
+ * moe_dispatch and moe_expert_ffn, the send buffer's chunk of each (rank, expert)
+ * pair (rows expert_start[e] .. + kept_counts[e]); a receiving rank lays its rows out
+ * expert by expert and calls moe_expert_ffn with a configuration of its local
+ * experts only (their counts and starts, their weights); the results go back to the
+ * rows they came from before moe_combine.  The Python package's ep module does this
+ * with point-to-point messages.
  *
  * Conventions (all calls):
  *   - Every pointer argument is a DEVICE pointer unless its comment says "host".
