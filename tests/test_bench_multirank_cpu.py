@@ -129,3 +129,18 @@ def test_launch_count_per_step():
     from expert_routing_router_b300 import workloads as W
     assert bench.launches_per_step(W.DSV3_PREFILL) == 9
     assert bench.launches_per_step(W.SWITCH_TOP1) == 8
+
+
+@pytest.mark.parametrize("tokens", [1, 2, 5])
+def test_cpu_baseline_sample_never_exceeds_the_batch(tokens):
+    """The oracle's timing sample (calibration included) stays inside the batch, down to
+    a one-token decode batch."""
+    from expert_routing_router_b300 import workloads as W
+    w = W.Workload("decode_like", tokens, 64, 8, 2, 2, 0, 1, True, 2, 1, 0.0, 32, 16, "bf16",
+                   0.0, 0.1, 1e-3)
+    h = bench.oracle_inputs(W.make_inputs(w, seed=3, device="cpu"))
+    import oracle
+    n = bench.oracle_sample_size(oracle, w, h, budget_s=0.5)
+    assert 1 <= n <= tokens
+    cb = bench.cpu_baseline(w, h, budget_s=0.5)
+    assert cb["value"] > 0 and f"of {tokens} tokens" in cb["sample"]
