@@ -29,6 +29,11 @@ Two transports move the chunks:
 The chunk sizes come from every rank's kept counts, gathered to the host once per step
 (ExchangePlan): the point-to-point sizes must be known where the operations are issued.
 The shared expert runs on the tokens' home rank (it sees every token) and is not sent.
+A buffer argument of the exchanges may be a tuple of row-aligned tensors (an INT8
+payload: codes [rows, d] int8 and scales [rows] fp32), moved chunk by chunk together.
+With a workload whose payload is "int8", the rank layer sends codes and scales both
+ways (moe_dispatch_q8 on the source, moe_dequant_rows and moe_quant_rows around the
+local experts on the receiver, moe_combine_q8 back on the source).
 """
 from dataclasses import replace
 
@@ -99,6 +104,10 @@ def gather_kept(kept_counts, group=None):
     return torch.stack(out).cpu().numpy()
 
 
+def _parts(buf):
+    return tuple(buf) if isinstance(buf, (tuple, list)) else (buf,)
+
+
 def exchange_dist(plan, send_buf, recv_buf, reverse=False, group=None):
     """One exchange through torch.distributed.  Forward: send_buf (this rank's send
     buffer) -> recv_buf (expert-major).  reverse=True: the results in recv_buf go back
@@ -106,32 +115,36 @@ def exchange_dist(plan, send_buf, recv_buf, reverse=False, group=None):
     and from this rank itself are copies.  Returns after every operation completed."""
     import torch.distributed as dist
     me = plan.me
-    # rank-to-rank order of the chunks: both sides walk one pair's chunks in expert order
+    sends, recvs = _parts(send_buf), _parts(recv_buf)
+    assert len(sends) == len(recvs)
+    # rank-to-rank order of the messages: both sides walk one pair's chunks in expert
+    # order, and the parts of a chunk in tuple order
     outgoing = [(dst, e, off, n) for (dst, e, off, n) in plan.send_chunks]
     incoming = {(src, e): (off, n) for (src, e, off, n) in plan.recv_chunks}
     ops = []
     if not reverse:
         for (dst, e, off, n) in outgoing:
             if n and dst != me:
-                ops.append(dist.P2POp(dist.isend, send_buf[off:off + n], dst, group))
+                ops += [dist.P2POp(dist.isend, t[off:off + n], dst, group) for t in sends]
         for (src, e, off, n) in plan.recv_chunks:
             if n and src != me:
-                ops.append(dist.P2POp(dist.irecv, recv_buf[off:off + n], src, group))
+                ops += [dist.P2POp(dist.irecv, t[off:off + n], src, group) for t in recvs]
     else:
         for (src, e, off, n) in plan.recv_chunks:
             if n and src != me:
-                ops.append(dist.P2POp(dist.isend, recv_buf[off:off + n], src, group))
+                ops += [dist.P2POp(dist.isend, t[off:off + n], src, group) for t in recvs]
         for (dst, e, off, n) in outgoing:
             if n and dst != me:
-                ops.append(dist.P2POp(dist.irecv, send_buf[off:off + n], dst, group))
+                ops += [dist.P2POp(dist.irecv, t[off:off + n], dst, group) for t in sends]
     for (dst, e, off, n) in outgoing:        # this rank's own experts
         if n and dst == me:
             roff, rn = incoming[(me, e)]
             assert rn == n
-            if not reverse:
-                recv_buf[roff:roff + n].copy_(send_buf[off:off + n])
-            else:
-                send_buf[off:off + n].copy_(recv_buf[roff:roff + n])
+            for ts, tr in zip(sends, recvs):
+                if not reverse:
+                    tr[roff:roff + n].copy_(ts[off:off + n])
+                else:
+                    ts[off:off + n].copy_(tr[roff:roff + n])
     if ops:
         for req in dist.batch_isend_irecv(ops):
             req.wait()
@@ -145,10 +158,11 @@ def exchange_loopback(plans, send_bufs, recv_bufs, reverse=False):
                 continue
             soff, sn = plans[src].send_offset(me, e)
             assert sn == n
-            if not reverse:
-                recv_bufs[me][roff:roff + n].copy_(send_bufs[src][soff:soff + n])
-            else:
-                send_bufs[src][soff:soff + n].copy_(recv_bufs[me][roff:roff + n])
+            for ts, tr in zip(_parts(send_bufs[src]), _parts(recv_bufs[me])):
+                if not reverse:
+                    tr[roff:roff + n].copy_(ts[soff:soff + n])
+                else:
+                    ts[soff:soff + n].copy_(tr[roff:roff + n])
 
 
 class RankLayer:
@@ -178,10 +192,18 @@ class RankLayer:
         self.recv_capacity = cap
         self.recv_x = torch.empty(cap, d, dtype=w.torch_dtype, device=device)
         self.recv_y = torch.empty(cap, d, dtype=w.torch_dtype, device=device)
+        self.int8 = getattr(w, "payload", "act") == "int8"
+        if self.int8:  # codes + scales travel; every received row holds an assignment
+            self.recv_xq = torch.empty(cap, d, dtype=torch.int8, device=device)
+            self.recv_xs = torch.empty(cap, dtype=torch.float32, device=device)
+            self.recv_yq = torch.empty(cap, d, dtype=torch.int8, device=device)
+            self.recv_ys = torch.empty(cap, dtype=torch.float32, device=device)
+            self.recv_valid = torch.zeros(cap, dtype=torch.int32, device=device)
         self.local_w = replace(w, name=f"{w.name}.experts{rank}", tokens=cap, top_k=1,
                                num_experts=len(self.local), num_ranks=1, rank_map=0,
                                num_groups=1, topk_groups=1, capacity_factor=0.0,
-                               shared_d_ff=0, sel_bias_std=0.0, dispatch_mode=0)
+                               shared_d_ff=0, sel_bias_std=0.0, dispatch_mode=0,
+                               payload="act")
         self.local_ws = torch.empty(moe.moe_workspace_size(moe.config(self.local_w)),
                                     dtype=torch.uint8, device=device)
         self.local_ws[:256].zero_()
@@ -193,9 +215,28 @@ class RankLayer:
         b, inp, c = self.b, self.inp, self.b.cfg
         moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"], inp["sel_bias"], b.logits,
                       b.topk_idx, b.topk_w, b.workspace, stream)
-        moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
-                         b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of, b.perm_src,
-                         b.num_kept, b.workspace, stream)
+        if self.int8:
+            moe.moe_dispatch_q8(c, b.topk_idx, inp["x"], b.xperm_q, b.xscale, b.expert_counts,
+                                b.kept_counts, b.expert_start, b.rank_counts, b.rank_offsets,
+                                b.slot_of, b.perm_src, b.num_kept, b.workspace, stream)
+        else:
+            moe.moe_dispatch(c, b.topk_idx, inp["x"], b.xperm, b.expert_counts, b.kept_counts,
+                             b.expert_start, b.rank_counts, b.rank_offsets, b.slot_of,
+                             b.perm_src, b.num_kept, b.workspace, stream)
+
+    # the buffers the two exchanges move: this rank's send / return rows, and its
+    # receive buffers (activations, or INT8 codes + scales)
+    def send_rows(self):
+        return (self.b.xperm_q, self.b.xscale) if self.int8 else self.b.xperm
+
+    def return_rows(self):
+        return (self.b.yperm_q, self.b.yscale) if self.int8 else self.b.yperm
+
+    def received_rows(self):
+        return (self.recv_xq, self.recv_xs) if self.int8 else self.recv_x
+
+    def result_rows(self):
+        return (self.recv_yq, self.recv_ys) if self.int8 else self.recv_y
 
     def check_plan(self, plan):
         if plan.recv_rows > self.recv_capacity:
@@ -203,14 +244,24 @@ class RankLayer:
                              f"receive buffers hold {self.recv_capacity}")
 
     def local_ffn(self, plan, stream=None):
-        """The local experts on the expert-major receive buffer (recv_x -> recv_y)."""
+        """The local experts on the expert-major receive buffer (recv_x -> recv_y); with
+        an INT8 payload the received codes are dequantised first and the results
+        quantised after."""
+        if not plan.recv_rows:
+            return
         self.local_start.copy_(torch.tensor(plan.local_start, dtype=torch.int32))
         self.local_kept.copy_(torch.tensor(plan.local_kept, dtype=torch.int32))
         # the kernel choice reads the average rows per expert from the configuration
-        cfg = moe.config(replace(self.local_w, tokens=max(plan.recv_rows, 1)))
+        cfg = moe.config(replace(self.local_w, tokens=plan.recv_rows))
+        if self.int8:
+            moe.moe_dequant_rows(cfg, self.recv_xq, self.recv_xs, self.recv_valid, self.recv_x,
+                                 stream)
         moe.moe_expert_ffn(cfg, self.recv_x, self.local_start, self.local_kept, self.w_gate_up,
                            self.w_down, None, None, None, self.recv_y, None, self.local_ws,
                            stream)
+        if self.int8:
+            moe.moe_quant_rows(cfg, self.recv_y, self.recv_valid, self.recv_yq, self.recv_ys,
+                               stream)
 
     def shared_ffn(self, stream=None):
         """The shared expert on this rank's own tokens (no routed rows)."""
@@ -223,7 +274,12 @@ class RankLayer:
 
     def combine(self, stream=None):
         b, inp = self.b, self.inp
-        moe.moe_combine(b.cfg, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out, stream)
+        if self.int8:
+            moe.moe_combine_q8(b.cfg, b.yperm_q, b.yscale, b.slot_of, b.topk_w, inp["x"],
+                               b.yshared, b.out, stream)
+        else:
+            moe.moe_combine(b.cfg, b.yperm, b.slot_of, b.topk_w, inp["x"], b.yshared, b.out,
+                            stream)
 
 
 def run_layer_loopback(ranks, bias_step=0.0):
@@ -239,10 +295,11 @@ def run_layer_loopback(ranks, bias_step=0.0):
     plans = [ExchangePlan(kept, w0.num_experts, R, w0.rank_map, me) for me in range(R)]
     for r, plan in zip(ranks, plans):
         r.check_plan(plan)
-    exchange_loopback(plans, [r.b.xperm for r in ranks], [r.recv_x for r in ranks])
+    exchange_loopback(plans, [r.send_rows() for r in ranks], [r.received_rows() for r in ranks])
     for r, plan in zip(ranks, plans):
         r.local_ffn(plan)
-    exchange_loopback(plans, [r.b.yperm for r in ranks], [r.recv_y for r in ranks], reverse=True)
+    exchange_loopback(plans, [r.return_rows() for r in ranks], [r.result_rows() for r in ranks],
+                      reverse=True)
     for r in ranks:
         r.shared_ffn()
         r.combine()
@@ -268,9 +325,9 @@ def run_layer_dist(rank_layer, group=None, bias_step=0.0):
     # rank all ranks take the same decision here and none is left waiting in an exchange
     for other in range(w.num_ranks):
         r.check_plan(ExchangePlan(kept, w.num_experts, w.num_ranks, w.rank_map, other))
-    exchange_dist(plan, r.b.xperm, r.recv_x, group=group)
+    exchange_dist(plan, r.send_rows(), r.received_rows(), group=group)
     r.local_ffn(plan)
-    exchange_dist(plan, r.b.yperm, r.recv_y, reverse=True, group=group)
+    exchange_dist(plan, r.return_rows(), r.result_rows(), reverse=True, group=group)
     r.shared_ffn()
     r.combine()
     if bias_step and r.inp["sel_bias"] is not None:

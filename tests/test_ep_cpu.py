@@ -109,6 +109,28 @@ def test_loopback_exchange_round_trip():
         assert torch.equal(back[r][kept_rows], want)
 
 
+def _scales(rows):
+    """A second, 1-D buffer aligned with the rows (as INT8 scales are with codes)."""
+    return (rows[:, 0] * 1000 + rows[:, 1]).to(torch.float32).contiguous()
+
+
+def test_loopback_exchange_of_row_aligned_pairs():
+    """A payload of two row-aligned tensors (codes + scales) moves chunk by chunk together."""
+    R, E, k, N, rm, cf = 2, 8, 2, 33, 0, 0.0
+    tabs = [_tables(r, N, E, k, R, rm, cf, 21) for r in range(R)]
+    kept = np.stack([t[1]["kept_counts"] for t in tabs])
+    plans = [ep.ExchangePlan(kept, E, R, rm, me) for me in range(R)]
+    send = [torch.from_numpy(_send_rows(r, *tabs[r], k)) for r in range(R)]
+    pairs = [(s_, _scales(s_)) for s_ in send]
+    recv = [(torch.full((max(p.recv_rows, 1), 4), -7.0, dtype=torch.float64),
+             torch.full((max(p.recv_rows, 1),), -7.0)) for p in plans]
+    ep.exchange_loopback(plans, pairs, recv)
+    for me, p in enumerate(plans):
+        _check_received(me, p, recv[me][0], tabs, k)
+        rows = p.recv_rows
+        assert torch.equal(recv[me][1][:rows], _scales(recv[me][0][:rows]))
+
+
 def _check_received(me, plan, recv, tabs, k):
     for (src, e, off, n) in plan.recv_chunks:
         idx, d = tabs[src]
@@ -134,6 +156,11 @@ def _worker(rank, world, port, case, q):
         recv = torch.full((max(plan.recv_rows, 1), 4), -7.0, dtype=torch.float64)
         ep.exchange_dist(plan, send, recv)
         _check_received(rank, plan, recv, tabs, k)
+        # a row-aligned pair (as INT8 codes + scales) takes the same path
+        recv2 = (torch.full_like(recv, -3.0), torch.full((recv.shape[0],), -3.0))
+        ep.exchange_dist(plan, (send, _scales(send)), recv2)
+        assert torch.equal(recv2[0][:plan.recv_rows], recv[:plan.recv_rows])
+        assert torch.equal(recv2[1][:plan.recv_rows], _scales(recv[:plan.recv_rows]))
         res = recv.clone()
         res[:, 3] += 1000.0                              # the "expert" marks its result
         back = torch.full_like(send, -5.0)

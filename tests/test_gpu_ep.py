@@ -114,3 +114,36 @@ def test_expert_parallel_layer_dist_single_rank():
     sgn = np.sign(counts * w.num_experts - w.tokens * w.top_k)
     ref = (host(sb0) - np.float32(w.bias_step) * sgn.astype(np.float32)).astype(np.float32)
     np.testing.assert_array_equal(host(whole["sel_bias"]), ref)
+
+
+def test_expert_parallel_int8_payload_matches_the_single_device_layer():
+    """INT8 codes + scales cross both exchanges (dispatch_q8 on the source, dequant and
+    quant around the local experts, combine_q8 back home).  Each rank's layer is compared
+    with the single-device INT8 layer on the same tokens: the routing, the send codes
+    and scales bit for bit, and the output within the bf16 layer tolerance (the expert
+    rows are the same products in the same order, grouped into other tiles)."""
+    from expert_routing_router_b300 import moe
+    w = small(tokens=300, hidden=264, num_experts=16, top_k=4, num_ranks=2, d_ff=200,
+              shared_d_ff=72, bias_step=0.0, payload="int8")
+    ranks, whole = _ranks(w, 2, seed=6)
+    ep.run_layer_loopback(ranks)
+    torch.cuda.synchronize()
+    for r, rank in enumerate(ranks):
+        assert int(rank.b.workspace[:4].view(torch.int32).item()) == 0
+        one = moe.LayerBuffers(w)
+        moe.run_layer(one, rank.inp)
+        torch.cuda.synchronize()
+        for name in ("topk_idx", "slot_of", "perm_src", "kept_counts"):
+            np.testing.assert_array_equal(host(getattr(rank.b, name)), host(getattr(one, name)),
+                                          err_msg=name)
+        kept = np.nonzero(host(one.perm_src) >= 0)[0]
+        rows = torch.from_numpy(kept).cuda().long()
+        np.testing.assert_array_equal(host(rank.b.xperm_q[rows]), host(one.xperm_q[rows]))
+        np.testing.assert_array_equal(host(rank.b.xscale[rows]), host(one.xscale[rows]))
+        got = rank.b.out.double().cpu().numpy()
+        ref = one.out.double().cpu().numpy()
+        x = rank.inp["x"].double().cpu().numpy()
+        # the MoE part (out - x) within 2e-2 of its own scale, plus the storage rounding of
+        # out, so that an error in the exchanged expert rows cannot hide behind the residual
+        allow = 2e-2 * np.max(np.abs(ref - x)) + 2.0 ** -8 * np.abs(ref)
+        assert np.all(np.abs((got - x) - (ref - x)) <= allow)
