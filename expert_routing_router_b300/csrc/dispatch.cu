@@ -33,13 +33,16 @@ __device__ __forceinline__ int64_t assignment_of(int64_t p, int N, int k, int mo
   return mode == MOE_DISPATCH_CAPACITY_PADDED ? (p % N) * k + p / N : p;
 }
 
-__global__ void __launch_bounds__(T2)
-count_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, int mode,
-             int32_t* __restrict__ chunk_hist, int32_t* __restrict__ perm_src, int64_t send_rows) {
+// The three passes are device functions of a chunk index `blk` (of `nblk`), run as one
+// kernel each, or back to back by one CTA when the assignments fit in one chunk.
+__device__ __forceinline__ void count_pass(int blk, int nblk, const int32_t* __restrict__ idx,
+                                           int64_t A, int N, int k, int E, int mode,
+                                           int32_t* __restrict__ chunk_hist,
+                                           int32_t* __restrict__ perm_src, int64_t send_rows) {
   __shared__ int hist[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += T2) hist[e] = 0;
   __syncthreads();
-  const int64_t p0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t p0 = (int64_t)blk * kChunk;
   const int64_t p1 = min(p0 + kChunk, A);
   for (int64_t p = p0 + threadIdx.x; p < p1; p += T2) {
     const int e = idx[assignment_of(p, N, k, mode)];
@@ -48,11 +51,16 @@ count_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, in
   // padded layout: rows without an assignment hold -1 (the assign kernel, which runs
   // after this one, overwrites the kept rows)
   if (mode == MOE_DISPATCH_CAPACITY_PADDED)
-    for (int64_t r = (int64_t)blockIdx.x * T2 + threadIdx.x; r < send_rows;
-         r += (int64_t)gridDim.x * T2)
+    for (int64_t r = (int64_t)blk * T2 + threadIdx.x; r < send_rows; r += (int64_t)nblk * T2)
       perm_src[r] = -1;
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += T2) chunk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
+  for (int e = threadIdx.x; e < E; e += T2) chunk_hist[(int64_t)blk * E + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(T2)
+count_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, int mode,
+             int32_t* __restrict__ chunk_hist, int32_t* __restrict__ perm_src, int64_t send_rows) {
+  count_pass(blockIdx.x, gridDim.x, idx, A, N, k, E, mode, chunk_hist, perm_src, send_rows);
 }
 
 // Position of expert e in the send order (rank ascending, expert ascending).
@@ -65,12 +73,14 @@ __device__ __forceinline__ int send_pos(int e, int E, int R, int rank_map) {
   return e;
 }
 
-__global__ void __launch_bounds__(T2)
-scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int R, int rank_map, int C,
-            int mode,
-            int32_t* __restrict__ expert_counts, int32_t* __restrict__ kept_counts,
-            int32_t* __restrict__ expert_start, int32_t* __restrict__ rank_counts,
-            int32_t* __restrict__ rank_offsets, int32_t* __restrict__ num_kept) {
+__device__ __forceinline__ void scan_pass(int32_t* __restrict__ chunk_hist, int n_chunks, int E,
+                                          int R, int rank_map, int C, int mode,
+                                          int32_t* __restrict__ expert_counts,
+                                          int32_t* __restrict__ kept_counts,
+                                          int32_t* __restrict__ expert_start,
+                                          int32_t* __restrict__ rank_counts,
+                                          int32_t* __restrict__ rank_offsets,
+                                          int32_t* __restrict__ num_kept) {
   __shared__ int kept_by_pos[kMaxExperts];
   __shared__ int start_by_pos[kMaxExperts + 1];
   __shared__ int warp_tot[T2 / 32];
@@ -127,16 +137,28 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int R, int ra
 }
 
 __global__ void __launch_bounds__(T2)
-assign_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, int C, int mode,
-              const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ expert_start,
-              const int32_t* __restrict__ num_kept, int32_t* __restrict__ slot_of,
-              int32_t* __restrict__ perm_src) {
+scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int R, int rank_map, int C,
+            int mode,
+            int32_t* __restrict__ expert_counts, int32_t* __restrict__ kept_counts,
+            int32_t* __restrict__ expert_start, int32_t* __restrict__ rank_counts,
+            int32_t* __restrict__ rank_offsets, int32_t* __restrict__ num_kept) {
+  scan_pass(chunk_hist, n_chunks, E, R, rank_map, C, mode, expert_counts, kept_counts,
+            expert_start, rank_counts, rank_offsets, num_kept);
+}
+
+__device__ __forceinline__ void assign_pass(int blk, const int32_t* __restrict__ idx, int64_t A,
+                                            int N, int k, int E, int C, int mode,
+                                            const int32_t* __restrict__ chunk_base,
+                                            const int32_t* __restrict__ expert_start,
+                                            const int32_t* __restrict__ num_kept,
+                                            int32_t* __restrict__ slot_of,
+                                            int32_t* __restrict__ perm_src) {
   __shared__ int run[kMaxExperts];
   __shared__ int wcnt[T2 / 32][kMaxExperts];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t a0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t a0 = (int64_t)blk * kChunk;
   const int64_t a1 = min(a0 + kChunk, A);
-  for (int e = tid; e < E; e += T2) run[e] = chunk_base[(int64_t)blockIdx.x * E + e];
+  for (int e = tid; e < E; e += T2) run[e] = chunk_base[(int64_t)blk * E + e];
   for (int64_t a = a0; a < a1; a += T2) {
     for (int q = tid; q < (T2 / 32) * E; q += T2) wcnt[q / E][q % E] = 0;
     __syncthreads();  // also orders run[] updates of the previous round
@@ -180,6 +202,35 @@ assign_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, i
     for (int64_t s = a0 + tid; s < a1; s += T2)
       if (s >= nk) perm_src[s] = -1;
   }
+}
+
+__global__ void __launch_bounds__(T2)
+assign_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, int C, int mode,
+              const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ expert_start,
+              const int32_t* __restrict__ num_kept, int32_t* __restrict__ slot_of,
+              int32_t* __restrict__ perm_src) {
+  assign_pass(blockIdx.x, idx, A, N, k, E, C, mode, chunk_base, expert_start, num_kept, slot_of,
+              perm_src);
+}
+
+// All of count, scan and assign for assignments that fit in one chunk (decode-sized
+// batches): one CTA, the passes separated by block barriers (a pass's global writes
+// are visible to the whole block after the barrier), one launch instead of three.
+__global__ void __launch_bounds__(T2)
+count_scan_assign_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, int R,
+                         int rank_map, int C, int mode, int32_t* __restrict__ chunk_hist,
+                         int32_t* __restrict__ expert_counts, int32_t* __restrict__ kept_counts,
+                         int32_t* __restrict__ expert_start, int32_t* __restrict__ rank_counts,
+                         int32_t* __restrict__ rank_offsets, int32_t* __restrict__ num_kept,
+                         int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_src,
+                         int64_t send_rows) {
+  count_pass(0, 1, idx, A, N, k, E, mode, chunk_hist, perm_src, send_rows);
+  __syncthreads();
+  scan_pass(chunk_hist, 1, E, R, rank_map, C, mode, expert_counts, kept_counts, expert_start,
+            rank_counts, rank_offsets, num_kept);
+  __syncthreads();
+  assign_pass(0, idx, A, N, k, E, C, mode, chunk_hist, expert_start, num_kept, slot_of,
+              perm_src);
 }
 
 // K3: one CTA walks tokens; each 16-byte vector of a row is loaded once and stored
@@ -239,13 +290,21 @@ cudaError_t launch_dispatch(const Cfg& c, const int32_t* topk_idx, const void* x
                             int32_t* rank_counts, int32_t* rank_offsets, int32_t* slot_of,
                             int32_t* perm_src, int32_t* num_kept, int32_t* chunk_hist,
                             cudaStream_t s) {
-  count_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.N, c.k, c.E, c.mode, chunk_hist,
-                                         perm_src, c.send_rows);
-  scan_kernel<<<1, T2, 0, s>>>(chunk_hist, c.n_chunks, c.E, c.R, c.rank_map, c.C, c.mode,
-                               expert_counts, kept_counts, expert_start, rank_counts,
-                               rank_offsets, num_kept);
-  assign_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.N, c.k, c.E, c.C, c.mode, chunk_hist,
-                                          expert_start, num_kept, slot_of, perm_src);
+  if (c.n_chunks == 1) {
+    count_scan_assign_kernel<<<1, T2, 0, s>>>(topk_idx, c.A, c.N, c.k, c.E, c.R, c.rank_map, c.C,
+                                              c.mode, chunk_hist, expert_counts, kept_counts,
+                                              expert_start, rank_counts, rank_offsets, num_kept,
+                                              slot_of, perm_src, c.send_rows);
+  } else {
+    count_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.N, c.k, c.E, c.mode, chunk_hist,
+                                           perm_src, c.send_rows);
+    scan_kernel<<<1, T2, 0, s>>>(chunk_hist, c.n_chunks, c.E, c.R, c.rank_map, c.C, c.mode,
+                                 expert_counts, kept_counts, expert_start, rank_counts,
+                                 rank_offsets, num_kept);
+    assign_kernel<<<c.n_chunks, T2, 0, s>>>(topk_idx, c.A, c.N, c.k, c.E, c.C, c.mode,
+                                            chunk_hist, expert_start, num_kept, slot_of,
+                                            perm_src);
+  }
   if (xperm) {
     const int nvec = (int)((int64_t)c.d * c.act_bytes / 16);
     int grid = num_sms() * 8;
