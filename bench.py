@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                     help="override a workload field (e.g. num_experts=16), for small "
                          "profiling cases of the same kernels")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the decode sweep and the smaller layers (extra keys)")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the C-ABI calls every step instead of replaying a CUDA graph")
     return ap.parse_args()
@@ -183,38 +185,69 @@ def oracle_inputs(inp):
 
 
 def oracle_step(oracle, w, h, n):
-    """One layer pass of the oracle over the first n tokens, as a batch of n."""
-    x = h["x"][:n]
+    """One layer pass of the oracle on this host's cores.  Routing is per batch, so
+    the router, top-k selection, dispatch tables and bias update run over all N
+    tokens; the expert FFN and the combine are per token and run on the first n
+    tokens (with the full batch's routing).  Returns (seconds of the full-N part,
+    seconds of the n-token part)."""
+    t0 = time.perf_counter()
+    x = h["x"]
     logits = oracle.router_logits(x, h["w_router"], h["b_router"])
     idx, wts = oracle.route(logits, w.top_k, w.score_fn, w.normalize_topk, w.num_groups,
                             w.topk_groups, h["sel_bias"])
     d = oracle.dispatch(idx, w.num_experts, w.num_ranks, w.rank_map, w.capacity_factor,
                         w.dispatch_mode)
+    t1 = time.perf_counter()
     oracle.layer_tokens(np.arange(n, dtype=np.int32), x, idx, wts, d["slot_of"],
                         h["w_gate_up"], h["w_down"], h["shared_gate_up"], h["shared_down"])
+    t2 = time.perf_counter()
     if w.bias_step and h["sel_bias"] is not None:
-        oracle.bias_update(d["expert_counts"], h["sel_bias"], n, w.top_k, w.bias_step)
+        oracle.bias_update(d["expert_counts"], h["sel_bias"], w.tokens, w.top_k, w.bias_step)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2), t2 - t1
 
 
 def oracle_sample_size(oracle, w, h, budget_s):
-    """Largest token sample whose oracle pass fits in about budget_s seconds (the
-    oracle runs tokens in parallel, so calibrate with one token per host thread)."""
+    """Tokens of the per-token part (expert FFN + combine) that fit in about budget_s
+    seconds (tokens run in parallel, so calibrate with one token per host thread)."""
     n = min(w.tokens, max(2, oracle.num_threads()))
-    t0 = time.perf_counter()
-    oracle_step(oracle, w, h, n)
-    per_tok = (time.perf_counter() - t0) / n
-    return int(max(1, min(w.tokens, budget_s / max(per_tok, 1e-9))))
+    _, t = oracle_step(oracle, w, h, n)
+    return int(max(1, min(w.tokens, budget_s / max(t / n, 1e-9))))
+
+
+def oracle_rate(w, full_s, part_s, n):
+    """Tokens/s of one full layer pass: the full-N part as timed, the per-token part
+    scaled from n tokens to N."""
+    return w.tokens / (full_s + part_s * w.tokens / n)
+
+
+def oracle_sample_text(w, n):
+    return (f"{w.name}: router, top-k selection, dispatch tables and bias update over all "
+            f"{w.tokens} tokens; expert FFN + combine (per token) on the first {n} tokens, "
+            f"time scaled by {w.tokens}/{n}; fp64 CPU oracle")
 
 
 def cpu_baseline(w, h, budget_s=15.0):
     import oracle
     n = oracle_sample_size(oracle, w, h, budget_s)
-    t0 = time.perf_counter()
-    oracle_step(oracle, w, h, n)
-    dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"first {n} of {w.tokens} tokens of {w.name} as one batch: fp64 router, "
-                      f"routing, dispatch, SwiGLU experts and combine ({dt:.1f} s)"}
+    full_s, part_s = oracle_step(oracle, w, h, n)
+    return {"value": oracle_rate(w, full_s, part_s, n), "unit": "tokens/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": oracle_sample_text(w, n) + f" ({full_s + part_s:.1f} s)"}
+
+
+def bench_config(w, a, world, graph=True):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
+            "num_experts": w.num_experts, "top_k": w.top_k, "num_ranks": w.num_ranks,
+            "d_ff": w.d_ff, "shared_d_ff": w.shared_d_ff,
+            "capacity_factor": w.capacity_factor, "seed": a.seed,
+            "l2": "flushed between steps (252 MiB write outside the step events); "
+                  "per-step working set larger than L2",
+            "parallelism": f"replica x{world} (token-sharded; forward path without "
+                           "collectives; with several replicas one [E] int32 all-reduce "
+                           "of expert_counts feeds the bias update)",
+            "launch": "one CUDA graph per C-ABI call" if graph else "direct C-ABI calls"}
 
 
 # ------------------------------------------------------------------ native arm
@@ -254,8 +287,15 @@ def capture_layer(moe, b, inp, bias_step, reduce, world):
 
 
 def launches_per_step(w):
-    n = 1                      # route
-    n += 4                     # dispatch: count, scan, assign, permute
+    """Kernels of this library that one forward step launches."""
+    if w.act_dtype == "f32":
+        n = 1                  # route: fused logits + selection
+    elif w.tokens <= 16:
+        n = 2                  # route: CUDA-core logits, selection
+    else:
+        n = 3                  # route: router weight split, tensor-core logits, selection
+    one_chunk = w.tokens * w.top_k <= 2048
+    n += 2 if one_chunk else 4  # dispatch: count/scan/assign (fused for one chunk), permute
     n += 2                     # expert FFN: gate_up and down grouped GEMMs
     n += 1                     # combine
     n += 1 if w.bias_step else 0
@@ -285,23 +325,10 @@ def algorithmic(w, num_kept):
     return dict(dispatch=dispatch_bytes, combine=combine_bytes, flops=flops, wire=wire)
 
 
-def run_native(a, w, rank, world, local):
-    from expert_routing_router_b300 import moe
-    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
-    torch.cuda.set_device(dev)
-    # every replica holds the same layer (weights, router, selection bias) and its own
-    # token batch
-    inp = W.make_inputs(w, seed=a.seed, device=dev)
-    if rank > 0:
-        inp["x"] = W.make_tokens(w, w.tokens, seed=a.seed + rank, device=dev)
-    b = moe.LayerBuffers(w, device=dev)
-    step_bias = w.bias_step
-    bias0 = None if inp["sel_bias"] is None else inp["sel_bias"].clone()
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-    s = torch.cuda.current_stream()
-
+def layer_stages(moe, b, inp, bias_step, cb):
+    """(name, C-ABI call) of one layer step in path order; the INT8-payload path sends
+    and returns codes.  cb: the configuration the bias update runs with."""
     c = b.cfg
-    # (name, C-ABI call) in path order; the INT8-payload path sends and returns codes
     stages = [("route", lambda: moe.moe_route(c, inp["x"], inp["w_router"], inp["b_router"],
                                               inp["sel_bias"], b.logits, b.topk_idx, b.topk_w,
                                               b.workspace))]
@@ -328,13 +355,125 @@ def run_native(a, w, rank, world, local):
     else:
         stages.append(("combine", lambda: moe.moe_combine(c, b.yperm, b.slot_of, b.topk_w,
                                                           inp["x"], b.yshared, b.out)))
+    if bias_step:
+        stages.append(("bias_update", lambda: moe.moe_bias_update(cb, b.expert_counts,
+                                                                  inp["sel_bias"], bias_step)))
+    return stages
+
+
+def time_forward(moe, w, inp, dev, flush, steps, warmup):
+    """Forward layer steps of workload w on inputs inp (one CUDA graph per C-ABI call,
+    CUDA events between the calls of each timed step, L2 flushed between steps outside
+    the events).  Returns (per-stage mean ms, LayerBuffers after the last step)."""
+    b = moe.LayerBuffers(w, device=dev)
+    has_bias = bool(w.bias_step) and inp["sel_bias"] is not None
+    bias0 = inp["sel_bias"].clone() if has_bias else None
+    stages = layer_stages(moe, b, inp, w.bias_step if has_bias else 0.0, b.cfg)
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for _, f in stages:
+            f()
+    torch.cuda.synchronize()
+    runs = []
+    for _, f in stages:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            f()
+        runs.append(g.replay)
+    for _ in range(warmup):
+        for r in runs:
+            r()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(runs) + 1)]
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(i & 0xff)
+        evs[i][0].record(s)
+        for j, r in enumerate(runs):
+            r()
+            evs[i][j + 1].record(s)
+    torch.cuda.synchronize()
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(runs))] for e in evs])
+    if has_bias:
+        inp["sel_bias"].copy_(bias0)
+    assert int(b.workspace[:4].view(torch.int32).item()) == 0, "device status word set"
+    return {n: float(v) for (n, _), v in zip(stages, per.mean(axis=0))}, b
+
+
+def sweep(a, moe, inp, dev, flush, pk):
+    """The other workloads, forward only, each on one GPU: the DeepSeek-V3 decode sweep
+    (the prefill layer's weights, fresh tokens at every batch size) with its expert
+    weight stream against the HBM peak, then the smaller layers."""
+    steps, warmup = 20, 5
+    out = {"decode": {}, "layers": {}}
+    s_b = 2
+    for T in W.DECODE_TOKENS:
+        w = W.DSV3_DECODE.with_tokens(T)
+        inp_t = dict(inp, x=W.make_tokens(w, T, seed=a.seed, device=dev))
+        st, b = time_forward(moe, w, inp_t, dev, flush, steps, warmup)
+        ms = sum(st.values())
+        touched = int((b.kept_counts > 0).sum().item())
+        wbytes = (touched * 3 * w.hidden * w.d_ff + 3 * w.hidden * w.shared_d_ff) * s_b
+        ffn_gbs = wbytes / (st["expert_ffn"] * 1e-3) / 1e9
+        out["decode"][str(T)] = {
+            "tokens_per_s": T / (ms * 1e-3), "ms_per_step": ms,
+            "stage_ms": st, "experts_touched": touched,
+            "expert_weight_bytes_per_step": wbytes,
+            "expert_ffn_weight_gbs": ffn_gbs, "expert_ffn_frac_of_hbm": ffn_gbs / pk["hbm"],
+            "step_weight_gbs": wbytes / (ms * 1e-3) / 1e9,
+            "step_frac_of_hbm": wbytes / (ms * 1e-3) / 1e9 / pk["hbm"]}
+        del b
+    for name in ("tiny_top2_f32", "switch_top1_bf16", "gshard_top2_skewed",
+                 "gshard_top2_padded", "dsv3_prefill_int8"):
+        w = W.WORKLOADS[name]
+        # the INT8-payload layer has the prefill layer's draws: reuse its inputs
+        inp_w = inp if name == "dsv3_prefill_int8" else W.make_inputs(w, seed=a.seed,
+                                                                      device=dev)
+        st, b = time_forward(moe, w, inp_w, dev, flush, steps, warmup)
+        ms = sum(st.values())
+        nk = int(b.num_kept.item())
+        alg = algorithmic(w, nk)
+        dc_ms = sum(v for n, v in st.items() if n in ("dispatch", "dequant", "quant", "combine"))
+        ffn_tf = alg["flops"] / (st["expert_ffn"] * 1e-3) / 1e12
+        out["layers"][name] = {
+            "tokens_per_s": w.tokens / (ms * 1e-3), "ms_per_step": ms, "stage_ms": st,
+            "dtype": "f32" if w.act_dtype == "f32" else "bf16",
+            "drop_rate": 1.0 - nk / (w.tokens * w.top_k),
+            "expert_ffn_tflops": ffn_tf,
+            "expert_ffn_frac_of_bf16_peak": (ffn_tf / pk["bf16"]) if w.act_dtype == "bf16"
+                                            else None,
+            "dispatch_combine_gbs": (alg["dispatch"] + alg["combine"]) / (dc_ms * 1e-3) / 1e9}
+        del b
+        if inp_w is not inp:
+            del inp_w
+        torch.cuda.empty_cache()
+    out["note"] = ("forward only, 20 timed steps after 5 warm-up steps each, one CUDA graph "
+                   "per C-ABI call, L2 flushed between steps; decode weight bytes = (experts "
+                   "that received rows + the shared expert) x 3 d F x 2 B")
+    return out
+
+
+def run_native(a, w, rank, world, local):
+    from expert_routing_router_b300 import moe
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    # every replica holds the same layer (weights, router, selection bias) and its own
+    # token batch
+    inp = W.make_inputs(w, seed=a.seed, device=dev)
+    if rank > 0:
+        inp["x"] = W.make_tokens(w, w.tokens, seed=a.seed + rank, device=dev)
+    b = moe.LayerBuffers(w, device=dev)
+    step_bias = w.bias_step
+    bias0 = None if inp["sel_bias"] is None else inp["sel_bias"].clone()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+
+    c = b.cfg
     has_bias = bool(step_bias) and inp["sel_bias"] is not None
     # the bias update applies the sign rule to the routed counts of all replicas
     reduce = counts_allreduce(world) if has_bias else None
     cb = moe.with_tokens(c, w.tokens * world) if world > 1 else c
-    if has_bias:
-        stages.append(("bias_update", lambda: moe.moe_bias_update(cb, b.expert_counts,
-                                                                  inp["sel_bias"], step_bias)))
+    stages = layer_stages(moe, b, inp, step_bias if has_bias else 0.0, cb)
     names = [n for n, _ in stages]
     n_st = len(stages)
 
@@ -485,17 +624,7 @@ def run_native(a, w, rank, world, local):
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": float(step_ms.mean()),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.act_dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
-                   "num_experts": w.num_experts, "top_k": w.top_k, "num_ranks": w.num_ranks,
-                   "d_ff": w.d_ff, "shared_d_ff": w.shared_d_ff,
-                   "capacity_factor": w.capacity_factor, "seed": a.seed,
-                   "l2": "flushed between steps (252 MiB write outside the step events); "
-                         "per-step working set larger than L2",
-                   "parallelism": f"replica x{world} (token-sharded; forward path without "
-                                  "collectives; with several replicas one [E] int32 all-reduce "
-                                  "of expert_counts feeds the bias update)",
-                   "launch": "one CUDA graph per C-ABI call" if not a.no_graph
-                             else "direct C-ABI calls"},
+        "config": bench_config(w, a, world, graph=not a.no_graph),
         "roofline": {"kernel": "expert grouped GEMMs (gate_up+SwiGLU, down) of moe_expert_ffn",
                      "bound": "tensor", "achieved": ffn_tflops, "peak": pk["bf16"],
                      "unit": "TFLOP/s", "frac": ffn_tflops / pk["bf16"],
@@ -526,6 +655,8 @@ def run_native(a, w, rank, world, local):
         fwd_bwd_ms = (out["ms_per_step"] - stage_ms["expert_ffn"] +
                       out["backward"]["expert_ffn_save_ms"] + out["backward"]["ms_per_step"])
         out["backward"]["train_step_tokens_per_s"] = w.tokens / (fwd_bwd_ms * 1e-3)
+    if (not a.no_sweep and world == 1 and w.name == "dsv3_prefill"):
+        out["sweep"] = sweep(a, moe, inp, dev, flush, pk)
     if getattr(w, "payload", "act") == "int8":
         out["cpu_baseline"] = None           # the oracle baseline times the bf16-payload layer
     elif rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -633,29 +764,31 @@ def time_backward(a, w, moe, b, inp, s, flush, pk):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(a, w):
-    """The CPU oracle as it stands, on this host's cores: same workload, metric, unit."""
+    """The CPU oracle as it stands, on this host's cores: same workload, config, metric
+    and unit as the native arm; each step is one layer pass with the per-token part on
+    a bounded sample (oracle_step)."""
     import oracle
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     h = oracle_inputs(W.make_inputs(w, seed=a.seed, device=dev))
-    budget = 120.0 / max(1, a.steps + a.warmup)
+    steps = max(1, a.steps + a.warmup)
+    full_s, _ = oracle_step(oracle, w, h, 1)
+    budget = max(0.5, 120.0 / steps - full_s)
     n = oracle_sample_size(oracle, w, h, budget)
     for _ in range(a.warmup):
         oracle_step(oracle, w, h, n)
-    t0 = time.perf_counter()
+    full, part = 0.0, 0.0
     for _ in range(a.steps):
-        oracle_step(oracle, w, h, n)
-    dt = time.perf_counter() - t0
-    value = n * a.steps / dt
-    sample = (f"each step: first {n} of {w.tokens} tokens of {w.name} as one batch through the "
-              f"fp64 CPU oracle (router, routing, dispatch, SwiGLU experts, combine)")
+        f, p = oracle_step(oracle, w, h, n)
+        full, part = full + f, part + p
+    value = oracle_rate(w, full, part, n)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"impl": "reference", "metric": "MoE-layer tokens/s", "value": value,
             "unit": "tokens/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
-            "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": w.tokens / value * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden,
-                       "num_experts": w.num_experts, "top_k": w.top_k, "sample_tokens": n},
+            "config": bench_config(w, a, world, graph=not a.no_graph),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": "each step: " + oracle_sample_text(w, n)},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

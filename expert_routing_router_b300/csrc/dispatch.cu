@@ -17,7 +17,6 @@
 //               within its expert -> slot or drop; perm_src tail cleared
 //   K3  permute every token row read once, written to each of its kept slots
 //               (16-byte vector loads / stores)
-#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -321,12 +320,12 @@ cudaError_t launch_dispatch(const Cfg& c, const int32_t* topk_idx, const void* x
 // histogram lives in one file-scope device array instead of the caller's workspace;
 // every GPU that loads this library keeps it (kNoAllocHistInts int32 = 256 KiB) until
 // the process exits.  Host code must not hand the array's name to a kernel (that is
-// a host-side stand-in, not a device address): its device address is looked up once
-// per device, with that device current, on the first call there.
+// a host-side stand-in, not a device address): every call looks up its device
+// address with the caller's device current.  The lookup is a host-side query, so a
+// context that was destroyed and created again (a device reset) gets the new
+// address on its next call instead of a stale one.
 namespace {
 static __device__ __align__(256) int32_t g_noalloc_hist[kNoAllocHistInts];
-std::mutex g_noalloc_mu;
-int32_t* g_noalloc_ptr[64];
 }  // namespace
 
 cudaError_t launch_dispatch_noalloc(const Cfg& c, const int32_t* topk_idx, const void* x,
@@ -334,25 +333,14 @@ cudaError_t launch_dispatch_noalloc(const Cfg& c, const int32_t* topk_idx, const
                                     int32_t* expert_start, int32_t* rank_counts,
                                     int32_t* rank_offsets, int32_t* slot_of, int32_t* perm_src,
                                     int32_t* num_kept, cudaStream_t s) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_hist);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int32_t* hist = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_noalloc_hist);
-      if (e != cudaSuccess) return e;
-      g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
-    }
-    hist = g_noalloc_ptr[dev];
-  }
   // The count kernel writes every histogram entry that the scan and assign kernels
   // read later, so nothing left over from an earlier call is ever used.
   return launch_dispatch(c, topk_idx, x, xperm, expert_counts, kept_counts, expert_start,
-                         rank_counts, rank_offsets, slot_of, perm_src, num_kept, hist, s);
+                         rank_counts, rank_offsets, slot_of, perm_src, num_kept,
+                         static_cast<int32_t*>(p), s);
 }
 
 }  // namespace moe

@@ -249,8 +249,12 @@ class RankLayer:
         quantised after."""
         if not plan.recv_rows:
             return
-        self.local_start.copy_(torch.tensor(plan.local_start, dtype=torch.int32))
-        self.local_kept.copy_(torch.tensor(plan.local_kept, dtype=torch.int32))
+        # the segment tables are written on the stream the kernels run on, so neither
+        # this step's kernels nor the previous step's can see them half written
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            self.local_start.copy_(torch.tensor(plan.local_start, dtype=torch.int32))
+            self.local_kept.copy_(torch.tensor(plan.local_kept, dtype=torch.int32))
         # the kernel choice reads the average rows per expert from the configuration
         cfg = moe.config(replace(self.local_w, tokens=plan.recv_rows))
         if self.int8:
@@ -331,7 +335,9 @@ def run_layer_dist(rank_layer, group=None, bias_step=0.0):
     r.shared_ffn()
     r.combine()
     if bias_step and r.inp["sel_bias"] is not None:
-        dist.all_reduce(r.b.expert_counts, group=group)
+        # summed into a copy: this rank's own routing counts stay in b.expert_counts
+        total = r.b.expert_counts.clone()
+        dist.all_reduce(total, group=group)
         cb = moe.with_tokens(r.b.cfg, w.tokens * w.num_ranks)
-        moe.moe_bias_update(cb, r.b.expert_counts, r.inp["sel_bias"], bias_step)
+        moe.moe_bias_update(cb, total, r.inp["sel_bias"], bias_step)
     return plan

@@ -180,11 +180,13 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, 
  * ceil(N*k / 2048) * num_experts int32) lives in a static device array of 65536
  * int32 (256 KiB) inside the library, which every GPU that loads the library keeps
  * until the process exits.  Larger layers are rejected with MOE_ERR_WORKSPACE (use
- * moe_dispatch).  The first call on a device looks up the array's device address
- * with that device current; make that first call before any stream capture.  All
- * calls share the one array: calls that overlap on the GPU (on different streams)
- * race and give wrong results.  Leftover contents from an earlier call are never
- * read, so nothing needs clearing.  Allocates nothing. */
+ * moe_dispatch).  Every call looks up the array's device address with the current
+ * device (a host-side query, so after a device reset the next call uses the new
+ * context's copy of the array); the first call on a device may load the library's
+ * device code there, so make it before any stream capture.  All calls share the one
+ * array: calls that overlap on the GPU (on different streams) race and give wrong
+ * results.  Leftover contents from an earlier call are never read, so nothing needs
+ * clearing.  Allocates nothing. */
 MOE_API moe_status moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx,
                                         const void* x, void* xperm, int32_t* expert_counts,
                                         int32_t* kept_counts, int32_t* expert_start,

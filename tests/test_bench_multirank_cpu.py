@@ -127,8 +127,13 @@ def test_reference_arm_nonzero_rank_exits_without_work():
 
 def test_launch_count_per_step():
     from expert_routing_router_b300 import workloads as W
-    assert bench.launches_per_step(W.DSV3_PREFILL) == 9
-    assert bench.launches_per_step(W.SWITCH_TOP1) == 8
+    # route: split + router GEMM + select; dispatch: count, scan, assign, permute;
+    # FFN: two grouped GEMMs; combine; bias update (the launch list of the prefill layer)
+    assert bench.launches_per_step(W.DSV3_PREFILL) == 11
+    assert bench.launches_per_step(W.SWITCH_TOP1) == 10
+    # one decode token: CUDA-core logits + select; one fused dispatch kernel + permute
+    assert bench.launches_per_step(W.DSV3_DECODE.with_tokens(1)) == 8
+    assert bench.launches_per_step(W.TINY_TOP2_F32) == 8
 
 
 @pytest.mark.parametrize("tokens", [1, 2, 5])
@@ -143,4 +148,7 @@ def test_cpu_baseline_sample_never_exceeds_the_batch(tokens):
     n = bench.oracle_sample_size(oracle, w, h, budget_s=0.5)
     assert 1 <= n <= tokens
     cb = bench.cpu_baseline(w, h, budget_s=0.5)
-    assert cb["value"] > 0 and f"of {tokens} tokens" in cb["sample"]
+    assert cb["value"] > 0 and f"all {tokens} tokens" in cb["sample"]
+    assert f"first {n} tokens" in bench.oracle_sample_text(w, n)
+    # the per-token part is scaled from the sample to the batch, the rest is not
+    assert bench.oracle_rate(w, 1.0, 2.0, tokens) == tokens / 3.0
