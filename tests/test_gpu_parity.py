@@ -12,9 +12,11 @@ isolates one kernel:
   layer             oracle fp64 layer from x and the weights        1e-4 (fp32) / 2e-2 (bf16)
   bias update       oracle fp32 sign rule                           bit-exact
 Tolerances are max-abs normalised: max|got - ref| <= tol * max|ref|.  Full-size
-workloads are checked on seeded samples of rows / tokens (always including every
-token whose choices were all dropped, up to a bound); the small cases are checked
-in full.
+workloads are checked on every expert's first and last send row and the rows on both
+sides of every 128-row tile border (the same for the shared expert's token rows), and
+the whole layer on a seeded sample of at least 1,024 tokens that always includes every
+token whose choices were all dropped; the small cases and the decode batches are
+checked in full.
 """
 import dataclasses
 
@@ -103,16 +105,36 @@ def check_route_dispatch(w, inp, b, rng, n_sample_tokens):
     return x_h, idx_gpu, w_ref, d, nk, kept_rows
 
 
-def sample_tokens(rng, N, n_sample_tokens, d, k):
-    """Token sample (or all), always including fully dropped tokens (up to 32)."""
+def sample_tokens(rng, N, n_sample_tokens, d, k, max_dropped=32):
+    """Token sample (or all), always including fully dropped tokens (up to max_dropped)."""
     slot = d["slot_of"].reshape(N, k)
     dropped = np.nonzero((slot < 0).all(axis=1))[0]
     if n_sample_tokens is None:
         toks = np.arange(N)
     else:
         toks = np.unique(np.concatenate([rng.choice(N, size=min(N, n_sample_tokens), replace=False),
-                                         dropped[:32]]))
+                                         dropped[:max_dropped]]))
     return toks.astype(np.int32), dropped
+
+
+TILE = 128  # row tile of the single-SM expert kernels; the SM-pair tiles (256) are multiples
+
+
+def border_rows(start, count, tile=TILE):
+    """Rows start..start+count-1 that a tiled kernel handles at an edge: the first and
+    last row, and the rows on both sides of every tile border inside the segment."""
+    if count <= 0:
+        return np.zeros(0, np.int64)
+    local = {0, count - 1}
+    for b in range(tile, count, tile):
+        local.update((b - 1, b))
+    return start + np.array(sorted(local), np.int64)
+
+
+def stratified_rows(expert_start, kept_counts):
+    """Send rows at the edges of every expert segment and of its row tiles."""
+    parts = [border_rows(int(s), int(c)) for s, c in zip(expert_start, kept_counts)]
+    return np.unique(np.concatenate(parts)) if parts else np.zeros(0, np.int64)
 
 
 # relative rounding of one store to the output type (round to nearest: half an ulp,
@@ -157,21 +179,31 @@ def check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0, hw=
     np.testing.assert_array_equal(xp, x_h[ps // k], err_msg="xperm")
     # ---- expert FFN on the GPU's send rows
     flat_idx = idx_gpu.reshape(-1)
-    sel = np.arange(nk) if n_sample_rows is None else np.sort(
-        rng.choice(nk, size=min(nk, n_sample_rows), replace=False))
+    if n_sample_rows == "borders":
+        # every expert segment's edges and row-tile borders, as positions in kept_rows
+        srows = stratified_rows(d["expert_start"], d["kept_counts"])
+        sel = np.searchsorted(kept_rows, srows)
+        assert np.array_equal(kept_rows[sel], srows)
+    else:
+        sel = np.arange(nk) if n_sample_rows is None else np.sort(
+            rng.choice(nk, size=min(nk, n_sample_rows), replace=False))
     wgu, wd, sgu, sd = hw["w_gate_up"], hw["w_down"], hw["shared_gate_up"], hw["shared_down"]
     if sel.size:
         y_ref = oracle.expert_rows(xp[sel], flat_idx[ps[sel]], wgu, wd)
         y_got = f64(b.yperm[torch.from_numpy(kept_rows[sel]).cuda().long()])
         close(y_got, y_ref, TOL_OUT[w.act_dtype], "expert FFN rows")
     if sgu is not None:
-        trows = np.arange(N) if n_sample_rows is None else np.sort(
-            rng.choice(N, size=min(N, n_sample_rows), replace=False))
+        if n_sample_rows == "borders":
+            trows = border_rows(0, N)
+        else:
+            trows = np.arange(N) if n_sample_rows is None else np.sort(
+                rng.choice(N, size=min(N, n_sample_rows), replace=False))
         ys_ref = oracle.expert_rows(x_h[trows], np.full(trows.size, E, np.int32), wgu, wd, sgu, sd)
         close(f64(b.yshared[torch.from_numpy(trows).cuda().long()]), ys_ref, TOL_OUT[w.act_dtype],
               "shared expert rows")
     # ---- combine from the GPU's yperm / weights, and the whole layer
-    toks, dropped = sample_tokens(rng, N, n_sample_tokens, d, k)
+    toks, dropped = sample_tokens(rng, N, n_sample_tokens, d, k,
+                                  max_dropped=N if n_sample_tokens is not None else 32)
     ys_h = None if b.yshared is None else host(b.yshared)
     out_got = f64(b.out)
     c_ref = oracle.combine(toks, x_h, host(b.yperm), d["slot_of"],
@@ -201,8 +233,13 @@ def check_layer_int8(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0
     N, k, E = w.tokens, w.top_k, w.num_experts
     x_h, idx_gpu, w_ref, d, nk, kept_rows = check_route_dispatch(w, inp, b, rng, n_sample_tokens)
     ps = d["perm_src"][kept_rows]
-    sel = np.arange(nk) if n_sample_rows is None else np.sort(
-        rng.choice(nk, size=min(nk, n_sample_rows), replace=False))
+    if n_sample_rows == "borders":
+        srows = stratified_rows(d["expert_start"], d["kept_counts"])
+        sel = np.searchsorted(kept_rows, srows)
+        assert np.array_equal(kept_rows[sel], srows)
+    else:
+        sel = np.arange(nk) if n_sample_rows is None else np.sort(
+            rng.choice(nk, size=min(nk, n_sample_rows), replace=False))
     rows = kept_rows[sel]
     rows_t = torch.from_numpy(rows).cuda().long()
     # ---- send payload: codes and scales of the kept tokens' rows
@@ -227,7 +264,8 @@ def check_layer_int8(w, inp, b, n_sample_tokens=None, n_sample_rows=None, seed=0
         np.testing.assert_array_equal(b.yscale[rows_t].cpu().numpy(), ys_ref,
                                       err_msg="return scales")
     # ---- combine from the GPU's return payload
-    toks, dropped = sample_tokens(rng, N, n_sample_tokens, d, k)
+    toks, dropped = sample_tokens(rng, N, n_sample_tokens, d, k,
+                                  max_dropped=N if n_sample_tokens is not None else 32)
     ys_h = None if b.yshared is None else host(b.yshared)
     out_got = f64(b.out)
     c_ref = oracle.combine_q8(toks, x_h, b.yperm_q.cpu().numpy(), b.yscale.cpu().numpy(),
@@ -291,7 +329,7 @@ def test_tiny_top2_f32_full():
 def test_capacity_workloads(w):
     inp = W.make_inputs(w, seed=0, device="cuda")
     b, _ = run_gpu(w, inp)
-    r = check_layer(w, inp, b, n_sample_tokens=256, n_sample_rows=256)
+    r = check_layer(w, inp, b, n_sample_tokens=1024, n_sample_rows="borders")
     C = oracle.capacity(w.tokens, w.top_k, w.num_experts, w.capacity_factor)
     assert host(b.kept_counts).max() <= C
     print(f"{w.name}: drop rate {r['drop_rate']:.4f}, layer rel err {r['rel_err']:.2e}")
@@ -301,7 +339,7 @@ def test_dsv3_prefill_and_bias_update(dsv3_inputs):
     from expert_routing_router_b300 import moe
     w, (inp, hw) = W.DSV3_PREFILL, dsv3_inputs
     b, bias0 = run_gpu(w, inp)
-    check_layer(w, inp, b, n_sample_tokens=48, n_sample_rows=128, hw=hw)
+    check_layer(w, inp, b, n_sample_tokens=1024, n_sample_rows="borders", hw=hw)
     counts = host(b.expert_counts)
     moe.moe_bias_update(b.cfg, b.expert_counts, inp["sel_bias"], w.bias_step)
     torch.cuda.synchronize()
@@ -342,7 +380,9 @@ def test_dsv3_decode_sweep(dsv3_inputs, T):
     inp = dict(dsv3_inputs[0])
     inp["x"] = W.make_tokens(w, T, seed=1, device="cuda")
     b, _ = run_gpu(w, inp)
-    check_layer(w, inp, b, n_sample_tokens=None if T <= 8 else 8, n_sample_rows=64,
+    # every token and every expert row up to 128 tokens; at 512 every token and the
+    # rows at each segment's edges and tile borders
+    check_layer(w, inp, b, n_sample_tokens=None, n_sample_rows=None if T <= 128 else "borders",
                 hw=dsv3_inputs[1])
 
 
@@ -519,7 +559,7 @@ def test_int8_payload_zero_and_extreme_rows():
 def test_dsv3_prefill_int8_payload(dsv3_inputs):
     w, (inp, hw) = W.DSV3_PREFILL_INT8, dsv3_inputs
     b, bias0 = run_gpu(w, inp)
-    check_layer(w, inp, b, n_sample_tokens=48, n_sample_rows=128, hw=hw)
+    check_layer(w, inp, b, n_sample_tokens=1024, n_sample_rows="borders", hw=hw)
     if bias0 is not None:
         inp["sel_bias"].copy_(bias0)
     del b
