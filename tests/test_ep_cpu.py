@@ -209,3 +209,148 @@ def test_receive_capacity_check_is_the_same_on_every_rank():
     with pytest.raises(ValueError, match="would receive 100 rows"):
         for other in range(R):
             Stub().check_plan(plans[other])
+
+
+# ---------------------------------------------------------------- source groups, overlap
+
+@pytest.mark.parametrize("R,G", [(2, 2), (4, 2), (4, 4), (3, 2), (5, 3)])
+def test_source_groups_cover_every_distance_once(R, G):
+    groups = ep.source_groups(R, G)
+    assert len(groups) == min(G, R)
+    assert sorted(j for g in groups for j in g) == list(range(R))
+    assert groups[0][0] == 0                    # a rank's own rows come first
+    assert all(g for g in groups)
+
+
+@pytest.mark.parametrize("case", CASES[:4], ids=lambda c: f"R{c['R']}E{c['E']}map{c['rank_map']}")
+@pytest.mark.parametrize("G", [2, 4])
+def test_grouped_plan_layout(case, G):
+    """Group-major receive layout: the same chunks as the plain plan, each source group
+    one block whose expert segments are contiguous, and both ends of every chunk agree
+    on the step that moves it."""
+    R, E, k, N, rm, cf = case["R"], case["E"], case["k"], case["N"], case["rank_map"], case["cf"]
+    tabs = [_tables(r, N, E, k, R, rm, cf, 7)[1] for r in range(R)]
+    kept = np.stack([t["kept_counts"] for t in tabs])
+    plain = [ep.ExchangePlan(kept, E, R, rm, me) for me in range(R)]
+    plans = [ep.ExchangePlan(kept, E, R, rm, me, groups=G) for me in range(R)]
+    for me, (p, q) in enumerate(zip(plans, plain)):
+        assert p.send_chunks == q.send_chunks and p.recv_rows == q.recv_rows
+        assert sorted((s, e, n) for (s, e, _, n) in p.recv_chunks) == \
+            sorted((s, e, n) for (s, e, _, n) in q.recv_chunks)
+        g_prev = 0
+        for g in range(p.G):
+            g0, g1 = p.group_rows[g]
+            assert g0 == g_prev
+            g_prev = g1
+            srcs = p.group_sources[g]
+            assert srcs == sorted((me - j) % R for j in p.dist_groups[g])
+            for i, e in enumerate(p.local_experts):
+                start, n = p.group_start[g][i], p.group_kept[g][i]
+                assert n == sum(kept[s, e] for s in srcs)
+                chunks = [(s, off, m) for (s, ee, off, m), st in zip(p.recv_chunks, p.recv_step)
+                          if ee == e and st == g]
+                assert [c[0] for c in chunks] == srcs     # sources ascending in a segment
+                off = g0 + start
+                for (s, o, m) in chunks:
+                    assert o == off
+                    off += m
+                assert off == g0 + start + n
+        assert g_prev == p.recv_rows
+        # the step that sends a chunk at its source is the step that receives it here
+        for (dst, e, _, n), st in zip(p.send_chunks, p.send_step):
+            other = plans[dst]
+            (j,) = [i for i, c in enumerate(other.recv_chunks) if c[0] == me and c[1] == e]
+            assert other.recv_step[j] == st
+
+
+@pytest.mark.parametrize("R,E,rm,G", [(2, 8, 0, 2), (4, 16, 1, 2), (3, 9, 1, 3)])
+def test_static_plan_is_the_padded_dispatch_layout(R, E, rm, G):
+    """With the capacity-padded send buffer the chunks are whole expert blocks of C rows
+    at the dispatch's expert_start: the plan needs no counts."""
+    k, N, cf = 2, 40, 1.0
+    for me in range(R):
+        idx = _routing(me, N, E, k, 3)
+        d = oracle.dispatch(idx, E, R, rm, cf, mode=1)
+        C = d["send_rows"] // E
+        p = ep.StaticExchangePlan(E, R, rm, me, C, groups=G)
+        assert p.send_rows == d["send_rows"]
+        for (dst, e, off, n) in p.send_chunks:
+            assert n == C and off == d["expert_start"][e]
+            assert e in ep.experts_of_rank(dst, E, R, rm)
+            # every kept row of the block lies in the chunk
+            assert d["kept_counts"][e] <= C
+        assert p.recv_rows == R * C * len(p.local_experts)
+        for g in range(p.G):
+            assert p.group_kept[g] == [C * len(p.group_sources[g])] * len(p.local_experts)
+
+
+def _overlap_worker(rank, world, port, case, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        R, E, k, N, rm, cf, G = world, case["E"], case["k"], case["N"], case["rank_map"], \
+            case["cf"], case["G"]
+        static = case.get("static", False)
+        tabs = [_tables(r, N, E, k, R, rm, cf, 11) for r in range(R)]
+        idx, d = tabs[rank]
+        if static:
+            idx_ = idx
+            d = oracle.dispatch(idx_, E, R, rm, cf, mode=1)
+            plan = ep.StaticExchangePlan(E, R, rm, rank, d["send_rows"] // E, groups=G)
+        else:
+            kept = ep.gather_kept(torch.from_numpy(d["kept_counts"].astype(np.int32)))
+            plan = ep.ExchangePlan(kept, E, R, rm, rank, groups=G)
+        send = torch.from_numpy(_send_rows(rank, idx, d, k))
+        recv = torch.full((max(plan.recv_rows, 1), 4), -7.0, dtype=torch.float64)
+        res = torch.full_like(recv, -9.0)
+        back = torch.full_like(send, -5.0)
+        done = []
+
+        def compute(g):                  # the "experts" of group g mark their rows
+            g0, g1 = plan.group_rows[g]
+            res[g0:g1] = recv[g0:g1]
+            res[g0:g1, 3] += 1000.0 * (g + 1)
+            done.append(g)
+        works = ep.overlapped_exchange(plan, send, recv, back, res, compute)
+        for wk in works:
+            wk.wait()
+        assert done == list(range(plan.G))
+        kept_rows = np.nonzero(d["perm_src"] >= 0)[0]
+        want = send[kept_rows].clone()
+        # each kept row came back from the group that holds its source (this rank) at
+        # the receiver, marked by that group
+        dst_of = {e: dst for dst in range(R) for e in ep.experts_of_rank(dst, E, R, rm)}
+        for i, s_row in enumerate(kept_rows):
+            e = int(send[s_row, 3])
+            j = (rank - dst_of[e]) % R            # my distance from the expert's owner
+            g = [gi for gi, js in enumerate(ep.source_groups(R, G)) if j in js][0]
+            want[i, 3] += 1000.0 * (g + 1)
+        assert torch.equal(back[kept_rows], want)
+        q.put((rank, "ok", plan.recv_rows))
+    except Exception as exc:                             # report, do not hang the peer
+        q.put((rank, repr(exc), -1))
+        raise
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("case", [dict(E=8, k=2, N=37, rank_map=0, cf=0.0, G=2),
+                                  dict(E=10, k=3, N=45, rank_map=1, cf=0.8, G=2),
+                                  dict(E=8, k=2, N=30, rank_map=0, cf=1.0, G=2, static=True)],
+                         ids=["contiguous", "round_robin_capacity", "static_padded"])
+def test_overlapped_exchange_gloo_two_ranks(case):
+    """The overlapped schedule of run_layer_dist (overlapped_exchange) between two gloo
+    ranks: group by group the rows reach the experts' owner, the owner's per-group
+    computation sees exactly that group's rows, and every result returns to its row."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 33500 + (os.getpid() % 2000) + case["E"] + 7 * case["k"] + (50 if case.get("static") else 0)
+    procs = [ctx.Process(target=_overlap_worker, args=(r, 2, port, case, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=180) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert [r[1] for r in res] == ["ok", "ok"], res
+    assert all(p.exitcode == 0 for p in procs)

@@ -17,14 +17,14 @@ from test_gpu_parity import check_layer, host, host_weights, small
 pytestmark = pytest.mark.gpu
 
 
-def _ranks(w, R, seed=0):
+def _ranks(w, R, seed=0, **kw):
     """R ranks of the layer: the same weights, each its own slice of the tokens."""
     whole = W.make_inputs(dataclasses.replace(w, tokens=w.tokens * R), seed=seed, device="cuda")
     ranks = []
     for r in range(R):
         inp = dict(whole)
         inp["x"] = whole["x"][r * w.tokens:(r + 1) * w.tokens].contiguous()
-        ranks.append(ep.RankLayer(w, r, inp))
+        ranks.append(ep.RankLayer(w, r, inp, **kw))
     return ranks, whole
 
 
@@ -147,3 +147,93 @@ def test_expert_parallel_int8_payload_matches_the_single_device_layer():
         # out, so that an error in the exchanged expert rows cannot hide behind the residual
         allow = 2e-2 * np.max(np.abs(ref - x)) + 2.0 ** -8 * np.abs(ref)
         assert np.all(np.abs((got - x) - (ref - x)) <= allow)
+
+
+# ---------------------------------------------------------------- overlapped schedule
+
+OVERLAP_CASES = {
+    # (workload, ranks, source groups, fixed plan on a capacity-padded send buffer)
+    "two_ranks_two_groups": (EP_CASES["two_ranks_contiguous_shared"][0], 2, 2, False),
+    "four_ranks_two_groups_round_robin_capacity":
+        (EP_CASES["four_ranks_round_robin_capacity"][0], 4, 2, False),
+    "four_ranks_four_groups_static": (small(tokens=300, hidden=136, num_experts=12, top_k=3,
+                                            num_ranks=4, rank_map=1, score_fn=0, num_groups=1,
+                                            topk_groups=1, capacity_factor=1.0, d_ff=96,
+                                            shared_d_ff=64, sel_bias_std=0.0,
+                                            dispatch_mode=1), 4, 4, True),
+    "two_ranks_static_int8": (small(tokens=300, hidden=264, num_experts=16, top_k=4,
+                                    num_ranks=2, capacity_factor=1.1, d_ff=200, shared_d_ff=72,
+                                    dispatch_mode=1, payload="int8"), 2, 2, True),
+    "dsv3_shape_two_ranks_two_groups": (EP_CASES["dsv3_shape_two_ranks"][0], 2, 2, False),
+}
+
+
+@pytest.mark.parametrize("name", list(OVERLAP_CASES))
+def test_expert_parallel_overlapped_schedule(name):
+    """The exchange and the local experts in steps over source groups, the copies on a
+    second stream (group g's expert FFN waits only for group g's rows; results go back
+    while the next group computes).  Each rank's layer is checked against the oracle,
+    and against the same rank's tokens as a single-device layer, bit for bit (every
+    expert row is the same products in the same order, whichever block it sits in)."""
+    from expert_routing_router_b300 import moe
+    w, R, G, static = OVERLAP_CASES[name]
+    ranks, whole = _ranks(w, R, seed=2, groups=G, static=static)
+    plans = ep.run_layer_loopback(ranks, overlap=True)
+    torch.cuda.synchronize()
+    assert plans[0].G == min(G, R)
+    hw = host_weights(whole)
+    for r, rank in enumerate(ranks):
+        assert int(rank.b.workspace[:4].view(torch.int32).item()) == 0
+        assert int(rank.local_ws[:4].view(torch.int32).item()) == 0
+        n_tok = None if w.tokens <= 1024 and w.hidden <= 1024 else 96
+        one = moe.LayerBuffers(w)
+        moe.run_layer(one, rank.inp)
+        torch.cuda.synchronize()
+        # with an INT8 payload the received rows live on the expert's rank, so the step
+        # by step check runs on the single-device layer, which this rank must equal
+        check_layer(w, rank.inp, one if w.payload == "int8" else rank.b,
+                    n_sample_tokens=n_tok,
+                    n_sample_rows=None if n_tok is None else "borders", seed=r, hw=hw)
+        assert torch.equal(rank.b.out, one.out), f"rank {r}: overlapped layer differs"
+
+
+def test_static_plan_moves_no_counts_and_repeats_exactly():
+    """The fixed plan is built once: two layer steps give identical outputs, and the
+    receive layout, split sizes and segment tables do not change between them."""
+    w, R, G, static = OVERLAP_CASES["four_ranks_four_groups_static"]
+    ranks, _ = _ranks(w, R, seed=5, groups=G, static=static)
+    tabs = [(r.g_start.clone(), r.g_kept.clone()) for r in ranks]
+    p1 = ep.run_layer_loopback(ranks, overlap=True)
+    torch.cuda.synchronize()
+    out1 = [r.b.out.clone() for r in ranks]
+    p2 = ep.run_layer_loopback(ranks, overlap=True)
+    torch.cuda.synchronize()
+    for r, rank in enumerate(ranks):
+        assert p1[r] is p2[r] is rank.static_plan
+        assert torch.equal(rank.g_start, tabs[r][0]) and torch.equal(rank.g_kept, tabs[r][1])
+        assert torch.equal(rank.b.out, out1[r])
+
+
+def test_expert_parallel_layer_dist_single_rank_static_plan():
+    """run_layer_dist with the fixed plan (capacity-padded send buffer) through an NCCL
+    group of one rank: no count exchange, every chunk a whole expert block."""
+    import socket
+    import torch.distributed as dist
+    w, _, _, _ = OVERLAP_CASES["four_ranks_four_groups_static"]
+    w = dataclasses.replace(w, num_ranks=1, rank_map=0)
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                            world_size=1)
+    try:
+        ranks, whole = _ranks(w, 1, seed=8, groups=2, static=True)
+        plan = ep.run_layer_dist(ranks[0])
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    r = ranks[0]
+    assert plan is r.static_plan and plan.G == 1
+    assert int(r.local_ws[:4].view(torch.int32).item()) == 0
+    check_layer(w, r.inp, r.b)
