@@ -304,6 +304,18 @@ def launches_per_step(w):
     return n
 
 
+def backward_launches(w):
+    """Kernels of this library that one timed backward step launches (the training form:
+    g, u and h saved by the forward)."""
+    n = 1                      # combine backward
+    n += 1 + 3 + 4 + 2         # expert FFN backward: padding plan, 3 padded copies,
+                               # dgrad D1/D2, wgrad W1/W2, zeroing of experts with no rows
+    n += 2                     # router backward: logit gradient, dx through the router
+    n += 4 if (w.act_dtype == "bf16" and w.tokens >= 128) else 1  # dW (split, GEMM, db x2)
+    n += 1                     # dispatch backward
+    return n
+
+
 def algorithmic(w, num_kept):
     """Bytes the dispatch / combine side must move, the expert flops, and the bytes an
     all-to-all would carry, for one step."""
@@ -707,7 +719,8 @@ def time_backward(a, w, moe, b, inp, s, flush, pk):
             g.workspace, saved=saved)),
         ("route_bwd", lambda: moe.moe_route_backward(c, inp["x"], inp["w_router"], b.logits,
                                                      b.topk_idx, g.dtopk_w, g.dlogits,
-                                                     g.dx_router, g.dw_router, g.db_router)),
+                                                     g.dx_router, g.dw_router, g.db_router,
+                                                     g.workspace)),
         ("dispatch_bwd", lambda: moe.moe_dispatch_backward(c, g.dxperm, b.slot_of, dout,
                                                            g.dx_shared, g.dx_router, g.dx)),
     ]
@@ -759,7 +772,7 @@ def time_backward(a, w, moe, b, inp, s, flush, pk):
                                "note": "dgrad + wgrad, 12 d F flops per row; h and g|u come "
                                        "from the training forward (moe_expert_ffn_save)"},
             "expert_ffn_save_ms": save_ms,
-            "clocks": clocks, "gpu_launches": 14 * a.steps, "device_status": status}
+            "clocks": clocks, "gpu_launches": backward_launches(w) * a.steps, "device_status": status}
 
 
 # ------------------------------------------------------------------ reference arm

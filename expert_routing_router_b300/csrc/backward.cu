@@ -18,7 +18,9 @@
 //                            (experts with dl = 0 skipped: k of E for renormalised or
 //                            sigmoid routing)
 //   router_dw_kernel         dWr and db: 8-expert x 256-column slices over all tokens,
-//                            skipping the tokens whose gradient is zero there
+//                            skipping the tokens whose gradient is zero there (fp32
+//                            layers and small batches; bf16 layers from 128 tokens use
+//                            the tensor-core GEMM of router_bwd_tc.cu)
 //   dispatch_bwd_kernel      one CTA per token: the gather-sum above
 //   zero_rows_kernel         zero the weight gradients of experts that received no rows
 #include "moe_internal.cuh"
@@ -388,7 +390,8 @@ cudaError_t launch_combine_backward(const Cfg& c, const void* dout, const void* 
 cudaError_t launch_route_backward(const Cfg& c, const void* x, const float* w_router,
                                   const float* logits, const int32_t* topk_idx,
                                   const float* dtopk_w, float* dlogits, float* dx_router,
-                                  float* dw_router, float* db_router, cudaStream_t s) {
+                                  float* dw_router, float* db_router, void* ws, int* status,
+                                  cudaStream_t s) {
   const int wg = (int)((c.N + TB / 32 - 1) / (TB / 32));
   route_bwd_kernel<<<wg < num_sms() * 8 ? wg : num_sms() * 8, TB, 0, s>>>(
       logits, topk_idx, dtopk_w, dlogits, c.N, c.E, c.k, c.score_fn, c.normalize ? 1 : 0);
@@ -398,6 +401,8 @@ cudaError_t launch_route_backward(const Cfg& c, const void* x, const float* w_ro
     router_dx_kernel<<<grid_rows(c.N), TB, 0, s>>>(dlogits, w_router, dx_router, c.N, c.E, c.d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (dw_router && ws && c.act == MOE_DTYPE_BF16 && c.N >= kRouterDwTcTokens)
+    return launch_router_dw_tc(c, dlogits, x, dw_router, db_router, ws, status, s);
   if (dw_router) {
     const dim3 grid((c.d + TB - 1) / TB, (c.E + DW_E - 1) / DW_E);
     if (c.act == MOE_DTYPE_F32)

@@ -442,7 +442,8 @@ moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
   moe_status st = make_cfg(cfg, &c);
   if (st != MOE_OK) return st;
   if (!bytes) return MOE_ERR_INVALID_ARG;
-  *bytes = 256 + round_up(ffn_backward_ws_bytes(c));
+  const size_t ffn = ffn_backward_ws_bytes(c), router = router_bwd_ws_bytes(c);
+  *bytes = 256 + round_up(ffn > router ? ffn : router);
   return MOE_OK;
 }
 
@@ -501,7 +502,8 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xperm,
 moe_status moe_route_backward(const moe_config* cfg, const void* x, const float* w_router,
                               const float* logits, const int32_t* topk_idx, const float* dtopk_w,
                               float* dlogits, float* dx_router, float* dw_router,
-                              float* db_router, void* stream) {
+                              float* db_router, void* workspace, size_t workspace_bytes,
+                              void* stream) {
   Cfg c;
   moe_status st = make_cfg(cfg, &c);
   if (st != MOE_OK) return st;
@@ -511,11 +513,21 @@ moe_status moe_route_backward(const moe_config* cfg, const void* x, const float*
   if (dx_router && (!w_router || !aligned(w_router, 16) || !aligned(dx_router, 16)))
     return MOE_ERR_INVALID_ARG;
   if ((dw_router == nullptr) != (db_router == nullptr)) return MOE_ERR_INVALID_ARG;
-  if (dw_router && (!x || !aligned(x, 16) || !aligned(dw_router, 4) || !aligned(db_router, 4)))
+  if (dw_router && (!x || !aligned(x, 16) || !aligned(dw_router, 16) || !aligned(db_router, 4)))
     return MOE_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  int* status = nullptr;
+  if (dw_router) {
+    size_t need = 0;
+    if ((st = moe_backward_workspace_size(cfg, &need)) != MOE_OK) return st;
+    if (!workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    status = static_cast<int*>(workspace);
+    ws = static_cast<char*>(workspace) + 256;
+  }
   if ((st = check_device()) != MOE_OK) return st;
   return from_cuda(launch_route_backward(c, x, w_router, logits, topk_idx, dtopk_w, dlogits,
-                                         dx_router, dw_router, db_router,
+                                         dx_router, dw_router, db_router, ws, status,
                                          static_cast<cudaStream_t>(stream)));
 }
 

@@ -154,7 +154,15 @@ cudaError_t launch_combine_backward(const Cfg& c, const void* dout, const void* 
 cudaError_t launch_route_backward(const Cfg& c, const void* x, const float* w_router,
                                   const float* logits, const int32_t* topk_idx,
                                   const float* dtopk_w, float* dlogits, float* dx_router,
-                                  float* dw_router, float* db_router, cudaStream_t s);
+                                  float* dw_router, float* db_router, void* ws, int* status,
+                                  cudaStream_t s);
+// The router's weight gradient on the tensor cores (router_bwd_tc.cu): dWr = dl^T x over
+// a 3-term bf16 split of dl, db by a fixed-order column sum.  ws: router_bwd_ws_bytes.
+size_t router_bwd_ws_bytes(const Cfg& c);
+cudaError_t launch_router_dw_tc(const Cfg& c, const float* dlogits, const void* x, float* dw_router,
+                                float* db_router, void* ws, int* status, cudaStream_t s);
+// Tokens from which a bf16 layer's router weight gradient runs on the tensor cores.
+constexpr int kRouterDwTcTokens = 128;
 cudaError_t launch_dispatch_backward(const Cfg& c, const void* dxperm, const int32_t* slot_of,
                                      const void* dout, const void* dx_shared,
                                      const float* dx_router, void* dx, cudaStream_t s);

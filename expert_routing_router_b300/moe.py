@@ -68,7 +68,7 @@ def _load():
     lib.moe_expert_ffn_backward.argtypes = [C] + [P] * 18 + [S, P]
     lib.moe_saved_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_expert_ffn_save.argtypes = [C] + [P] * 11 + [S, P, S, P]
-    lib.moe_route_backward.argtypes = [C] + [P] * 9 + [P]
+    lib.moe_route_backward.argtypes = [C] + [P] * 9 + [P, S, P]
     lib.moe_dispatch_backward.argtypes = [C] + [P] * 6 + [P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
@@ -251,10 +251,12 @@ def moe_expert_ffn_save(cfg, xperm, expert_start, kept_counts, w_gate_up, w_down
 
 
 def moe_route_backward(cfg, x, w_router, logits, topk_idx, dtopk_w, dlogits, dx_router,
-                       dw_router, db_router, stream=None):
+                       dw_router, db_router, workspace=None, stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("moe_route_backward", _lib.moe_route_backward(
         ctypes.byref(cfg), _p(x), _p(w_router), _p(logits), _p(topk_idx), _p(dtopk_w),
-        _p(dlogits), _p(dx_router), _p(dw_router), _p(db_router), _stream(stream)))
+        _p(dlogits), _p(dx_router), _p(dw_router), _p(db_router), _p(workspace), nbytes,
+        _stream(stream)))
 
 
 def moe_dispatch_backward(cfg, dxperm, slot_of, dout, dx_shared, dx_router, dx, stream=None):
@@ -303,7 +305,7 @@ def run_layer_backward(b, g, inp, dout, stream=None, saved=None):
                             g.dyperm, dout, g.dxperm, g.dx_shared, g.dw_gate_up, g.dw_down,
                             g.dshared_gate_up, g.dshared_down, g.workspace, stream, saved)
     moe_route_backward(c, inp["x"], inp["w_router"], b.logits, b.topk_idx, g.dtopk_w, g.dlogits,
-                       g.dx_router, g.dw_router, g.db_router, stream)
+                       g.dx_router, g.dw_router, g.db_router, g.workspace, stream)
     moe_dispatch_backward(c, g.dxperm, b.slot_of, dout, g.dx_shared, g.dx_router, g.dx, stream)
     return g.dx
 

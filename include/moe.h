@@ -383,14 +383,21 @@ MOE_API moe_status moe_expert_ffn_backward(const moe_config* cfg, const void* xp
  *   sigmoid, unnormalised:   dl_j = s_j (1 - s_j) dw_j
  * (s = the selection sigmoid of moe_route, p = softmax over all experts), then
  *   dx_router = dl . w_router  [N, hidden] fp32 (NULL to skip)
- *   dw_router = dl^T x [E, hidden] fp32 and db_router = sum_t dl [E] fp32 (both or
- *   neither NULL)
+ *   dw_router = dl^T x [E, hidden] fp32 (16-byte aligned) and db_router = sum_t dl
+ *   [E] fp32 (both or neither NULL)
  * logits [N, E] fp32 and topk_idx [N, k] from moe_route; dtopk_w from
- * moe_combine_backward; dlogits [N, E] fp32 out. */
+ * moe_combine_backward; dlogits [N, E] fp32 out.  workspace: the backward workspace
+ * (moe_backward_workspace_size bytes, 256-byte aligned; may be NULL when dw_router is
+ * NULL); its contents are not kept between calls, its first int32 is the device status
+ * word (nonzero if a kernel gave up a bounded wait).  With bf16 activations and at least
+ * 128 tokens dw_router is one tensor-core GEMM over an exact three-term bf16 split of dl
+ * (fp32 accumulation); db_router and the fp32 layers' dw_router are fixed-order fp32 sums
+ * over the tokens. */
 MOE_API moe_status moe_route_backward(const moe_config* cfg, const void* x, const float* w_router,
                                       const float* logits, const int32_t* topk_idx,
                                       const float* dtopk_w, float* dlogits, float* dx_router,
-                                      float* dw_router, float* db_router, void* stream);
+                                      float* dw_router, float* db_router, void* workspace,
+                                      size_t workspace_bytes, void* stream);
 
 /* Dispatch backward: the permute's transpose plus the residual, shared-expert and
  * router paths, summed in fp32 and rounded once:

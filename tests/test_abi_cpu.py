@@ -166,6 +166,14 @@ def test_backward_calls_validate_on_host(moe_lib):
         moe_lib.MOE_ERR_INVALID_ARG
     # router: dW and db come as a pair
     assert L.moe_route_backward(ctypes.byref(c3), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
-                                P(FAKE), None, P(FAKE), None, None) == moe_lib.MOE_ERR_INVALID_ARG
+                                P(FAKE), None, P(FAKE), None, P(FAKE), need,
+                                None) == moe_lib.MOE_ERR_INVALID_ARG
+    # router weight gradient: the backward workspace is required and checked for size
+    assert L.moe_route_backward(ctypes.byref(c3), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                P(FAKE), None, P(FAKE), P(FAKE), None, 0,
+                                None) == moe_lib.MOE_ERR_INVALID_ARG
+    assert L.moe_route_backward(ctypes.byref(c3), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                P(FAKE), None, P(FAKE), P(FAKE), P(FAKE), need - 1,
+                                None) == moe_lib.MOE_ERR_WORKSPACE
     assert L.moe_dispatch_backward(ctypes.byref(c3), P(FAKE), P(FAKE), None, None, None, P(FAKE),
                                    None) == moe_lib.MOE_ERR_INVALID_ARG
