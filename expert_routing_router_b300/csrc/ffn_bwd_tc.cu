@@ -20,19 +20,20 @@
 // TMA boxes, one 128-byte row per K index, descriptors with a leading offset of one
 // box (8 KiB) between 64-element MN chunks and 1 KiB between 8-row K groups, and the
 // instruction descriptor's transpose bit for that operand.
-// W1/W2 sum over a segment's rows, so a segment's rows must end in zeros up to the
-// next 64-row block (otherwise the last K block would add the next segment's rows, or
-// send-buffer rows never written).  The routed rows therefore live in a padded copy:
-// expert e's rows start at pad_start[e] (a prefix sum of its row count rounded up to
-// 64), and the rows up to that boundary are zero.  pad_rows_kernel copies xperm and
-// dY into that layout once per call; R1 and D1 then produce g, u, h and [dg | du] in it
-// (their padding rows come out zero, being products of zero rows).  The shared expert's
-// rows end where its tensors end, and TMA fills the rest of a block with zeros.
+// Every routed operand and result row is in the send-buffer layout (expert e's rows at
+// expert_start[e]).  W1/W2 sum over a segment's rows, so the last K block of a segment
+// must not add the next segment's rows (or send-buffer rows never written): in that
+// block only the K=16 MMAs that reach the segment's rows are issued, and the rows past
+// its end inside the last of them are zeroed by the MMA warp in both operands'
+// shared-memory tiles (whole 128-byte rows, so the swizzle does not matter) before the
+// MMA reads them.  The shared expert's rows end where its tensors end, and TMA fills the
+// rest of a block with zeros.
 // Experts with no rows get no W tiles; their gradients are zeroed by a separate kernel.
 // The W kinds' K loops are short (one segment's rows), so their output write is the
-// critical path: each tile is staged in shared memory (128-byte swizzle) and written
-// with TMA tensor stores into [segments, M, N] maps that clip a segment's row tail;
-// the ring has 3 stages there to make room.
+// critical path: every epilogue warp stages its 32 rows of each 64-column box in shared
+// memory (128-byte swizzle, two alternating 4 KB buffers per warp) and writes it with a
+// TMA tensor store into [segments, M, N] maps that clip a segment's row tail, without
+// waiting for the other warps; the ring has 3 stages there to make room.
 // Every mbarrier wait is bounded (about 2 s) and reports through the status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -46,8 +47,10 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int OUT_BYTES = BM * 64 * 2;  // W kinds: one 64-column box of the output tile,
-                                        // staged for a TMA store (four rounds per tile)
+// W kinds: every epilogue warp stages its 32 rows of one 64-column box of the output
+// tile (4 KB) for a TMA store, in two alternating buffers
+constexpr int WBOX_BYTES = 32 * 64 * 2;
+constexpr int OUT_BYTES = 4 * 2 * WBOX_BYTES;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -67,7 +70,7 @@ struct Traits {
   // W kinds: short K loops (a segment's rows) make the output write the critical path;
   // the tile goes out through a 16 KB shared-memory box and TMA stores
   static constexpr bool tma_out = k_rows;
-  static constexpr int stages = STAGES;
+  static constexpr int stages = k_rows ? 3 : STAGES;  // room for the staging buffers
   static constexpr uint32_t idesc =
       idesc_bf16_f32(BM, BN) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
 };
@@ -75,25 +78,22 @@ struct Traits {
 struct BwdParams {
   const int32_t* expert_start;
   const int32_t* kept_counts;
-  const int32_t* pad_start;  // [E + 1] padded row starts of the routed segments
   __nv_bfloat16* out0;  // routed output   R1 gu, D1 dgu, D2 dx, W1 dWd, W2 dWgu
   __nv_bfloat16* out1;  // shared output
   __nv_bfloat16* aux0;  // R1: h out (routed) / D1: gu in (routed)
   __nv_bfloat16* aux1;  // shared counterpart
   int* err;
   int E, n_shared, d, F, Fs;
-  int gu_send_layout;  // D1: routed g|u rows in the send-buffer layout (saved by the forward)
 };
 
 struct Ctl {
-  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, esync;
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
   uint32_t tmem_base;
   int abort;
   int tile_start[MAX_SEG + 1];
   int mtiles[MAX_SEG];
   int rows[MAX_SEG];
-  int row_base[MAX_SEG];  // first row in the (padded) operand layout
-  int out_base[MAX_SEG];  // first row of the segment in the send buffer (dX rows)
+  int row_base[MAX_SEG];  // first row of the segment in the send buffer (0: shared)
 };
 
 template <int KIND>
@@ -102,8 +102,8 @@ constexpr size_t smem_bytes() {
          (Traits<KIND>::tma_out ? OUT_BYTES : 0) + sizeof(Ctl);
 }
 
-// TMA store of one 64-column x 128-row box of a [segments, M, N] tensor (rows past a
-// segment's M are clipped by the map), then commit it to this thread's bulk group.
+// TMA store of one 64-column x 32-row box of a [segments, M, N] tensor (rows past a
+// segment's M are clipped by the map); the caller commits it to its bulk group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x,
                                              int y, int z) {
   asm volatile(
@@ -115,9 +115,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// the shared-memory sources of this thread's bulk stores have been read
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// the shared-memory sources of this thread's bulk stores, all but the latest group,
+// have been read
+__device__ __forceinline__ void bulk_wait_read_prev() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // this thread's bulk stores have completed
 __device__ __forceinline__ void bulk_wait_all() {
@@ -139,16 +140,6 @@ __device__ bool mbar_wait(uint64_t* b, uint32_t parity, Ctl* ctl, int* err, int 
       }
     }
   }
-}
-
-// Rendezvous of the 4 epilogue warps (an mbarrier, so that the wait is bounded like
-// every other): false if it expired or another role gave up.
-__device__ bool epi_sync(Ctl* ctl, uint32_t* phase, int* err) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->esync);
-  const bool ok = mbar_wait(&ctl->esync, *phase, ctl, err, 6);
-  *phase ^= 1;
-  return __all_sync(0xffffffffu, ok);
 }
 
 // MN-major 128-byte-swizzle descriptor: start >> 4, leading offset = one 64-element
@@ -177,7 +168,7 @@ template <int KIND>
 __device__ __forceinline__ int n_step() { return KIND == R1 ? BN / 2 : BN; }
 
 struct Tile {
-  int seg, m0, n0, M, N, K, row_base, out_base;
+  int seg, m0, n0, M, N, K, row_base;
   bool routed;
 };
 
@@ -206,7 +197,6 @@ __device__ __forceinline__ Tile decode(const Ctl* ctl, int nseg, int t, const Bw
     tl.n0 = (local / mt) * n_step<KIND>();
   }
   tl.row_base = ctl->row_base[lo];
-  tl.out_base = ctl->out_base[lo];
   return tl;
 }
 
@@ -237,7 +227,6 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       mbar_init(&ctl->tempty[a], 4);
     }
     mbar_init(&ctl->drain, 1);
-    mbar_init(&ctl->esync, 4);  // one arrival per epilogue warp
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -255,8 +244,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         const int mt = (M + BM - 1) / BM;
         ctl->mtiles[s] = mt > 0 ? mt : 1;
         ctl->rows[s] = cnt;
-        ctl->row_base[s] = routed ? p.pad_start[s] : 0;
-        ctl->out_base[s] = routed ? p.expert_start[s] : 0;
+        ctl->row_base[s] = routed ? p.expert_start[s] : 0;
         // a segment with no rows has nothing to compute (W kinds: its gradient is zeroed
         // elsewhere)
         v = (cnt > 0) ? mt * ((N + n_step<KIND>() - 1) / n_step<KIND>()) : 0;
@@ -360,12 +348,34 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           break;
         }
         uint8_t* sa = smem + (size_t)stage * STAGE_BYTES;
+        int kk_end = BK / 16;  // MMAs (K = 16 each) of this block
+        if (Tr::k_rows && tl.routed && k0 + BK > tl.K) {
+          // the segment ends inside this block: only the MMAs that reach its rows run,
+          // and the rows past its end inside the last of them (rows rem .. 16*kk_end-1
+          // of every box: 2 of A, 4 of B) are zeroed by the whole warp, whole 128-byte
+          // rows at a time, before the MMA reads them
+          const int rem = tl.K - k0;
+          kk_end = (rem + 15) >> 4;
+          const int zr1 = kk_end * 16;
+          if (rem < zr1) {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int box = 0; box < 6; ++box) {
+              uint8_t* base = box < 2 ? sa + box * BOX_BYTES : sa + A_BYTES + (box - 2) * BOX_BYTES;
+              for (int row = rem + (lane >> 3); row < zr1; row += 4)
+                *reinterpret_cast<uint4*>(base + row * 128 + (lane & 7) * 16) = z;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          __syncwarp();
+        }
         if (lane == 0) {
           tc_fence_after();
           const uint32_t a0 = saddr(sa);
           const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= kk_end) break;
             const uint64_t ad = Tr::a_mn ? sdesc_mn(a0 + kk * 2048) : sdesc(a0 + kk * 32);
             const uint64_t bd = Tr::b_mn ? sdesc_mn(b0 + kk * 2048) : sdesc(b0 + kk * 32);
             tc_mma(dt, ad, bd, Tr::idesc, (k0 > 0 || kk > 0) ? 1u : 0u);
@@ -397,17 +407,14 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
     int acc = 0;
-    uint32_t acc_phase = 0, esync_phase = 0;
+    uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode<KIND>(ctl, nseg, t, p);
       const int Fx = tl.routed ? p.F : p.Fs;
       if (!mbar_wait(&ctl->tfull[acc], acc_phase, ctl, p.err, 4)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      // R1 / D1 also store a routed segment's padding rows (zeros, from zero inputs),
-      // so that W1 / W2 read zeros there
-      const int m_store = ((KIND == R1 || KIND == D1) && tl.routed) ? ((tl.M + 63) & ~63) : tl.M;
-      const bool valid = tl.m0 + r < m_store;
+      const bool valid = tl.m0 + r < tl.M;
       __nv_bfloat16* out = tl.routed ? p.out0 : p.out1;
       if (KIND == R1) {
         // g in columns [0,128), u in [128,256): gu row (g at f, u at Fx + f) and h
@@ -450,12 +457,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       } else if (KIND == D1) {
         // dh columns [n0, n0+256): dg = dh u silu'(g), du = dh silu(g), from gu
         const int64_t row = tl.row_base + tl.m0 + r;
-        // padding rows (past the segment's rows) have dh = 0 and get zeros without
-        // reading g|u (the send-buffer layout has no such rows)
-        const bool real = tl.m0 + r < tl.M;
-        const int64_t grow =
-            ((p.gu_send_layout && tl.routed) ? tl.out_base : tl.row_base) + tl.m0 + r;
-        const __nv_bfloat16* gurow = (tl.routed ? p.aux0 : p.aux1) + grow * (2 * Fx);
+        const __nv_bfloat16* gurow = (tl.routed ? p.aux0 : p.aux1) + row * (2 * Fx);
         __nv_bfloat16* drow = out + row * (2 * Fx);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -467,9 +469,8 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             for (int v = 0; v < 4; ++v) {
               const int col = tl.n0 + c + v * 8;
               if (col >= Fx) continue;
-              const uint4 z4 = make_uint4(0, 0, 0, 0);
-              const uint4 gv = real ? *reinterpret_cast<const uint4*>(gurow + col) : z4;
-              const uint4 uv = real ? *reinterpret_cast<const uint4*>(gurow + Fx + col) : z4;
+              const uint4 gv = *reinterpret_cast<const uint4*>(gurow + col);
+              const uint4 uv = *reinterpret_cast<const uint4*>(gurow + Fx + col);
               const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
               const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
               uint32_t pdg[4], pdu[4];
@@ -495,12 +496,16 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
           }
         }
       } else if (Tr::tma_out) {
-        // [M, N] tile of dW, one 64-column box at a time: TMEM -> registers -> the 16 KB
-        // staging box (128-byte swizzle: 16-byte chunk j of row r at r*128 + (j^(r&7))*16)
-        // -> one TMA store.  Before writing the box, the previous store must have read it.
-        bool ok = true;
+        // [M, N] tile of dW, one 64-column box at a time: each warp moves its 32 rows
+        // TMEM -> registers -> its own 4 KB staging buffer (128-byte swizzle: 16-byte
+        // chunk j of row r at r*128 + (j^(r&7))*16) -> one TMA store, alternating two
+        // buffers so that staging a box overlaps the previous box's store; no warp waits
+        // for another.  Every box commits one bulk group (empty when the box lies past
+        // the last column), so waiting until all but the latest group have read their
+        // source frees the buffer about to be written.
+        uint8_t* wst = stage_out + (size_t)q * 2 * WBOX_BYTES;
 #pragma unroll 1
-        for (int bx = 0; bx < BN / 64 && ok; ++bx) {
+        for (int bx = 0; bx < BN / 64; ++bx) {
           uint32_t y[2][32];
           tmem_ld32(tb + 64 * bx, y[0]);
           tmem_ld32(tb + 64 * bx + 32, y[1]);
@@ -511,8 +516,9 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
           }
-          if (threadIdx.x == 64) bulk_wait_read();
-          if (!epi_sync(ctl, &esync_phase, p.err)) { ok = false; break; }
+          uint8_t* buf = wst + (size_t)(bx & 1) * WBOX_BYTES;
+          if (lane == 0) bulk_wait_read_prev();
+          __syncwarp();
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t pk[16];
@@ -522,19 +528,19 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               const int chunk = h2 * 4 + v;
-              *reinterpret_cast<uint4*>(stage_out + r * 128 + ((chunk ^ (r & 7)) << 4)) =
+              *reinterpret_cast<uint4*>(buf + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
                   make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          if (!epi_sync(ctl, &esync_phase, p.err)) { ok = false; break; }
-          if (threadIdx.x == 64 && tl.n0 + 64 * bx < tl.N) {
-            tma_store_3d(tl.routed ? &tmO0 : &tmO1, stage_out, tl.n0 + 64 * bx, tl.m0,
-                         tl.routed ? tl.seg : 0);
+          __syncwarp();
+          if (lane == 0) {
+            if (tl.n0 + 64 * bx < tl.N)
+              tma_store_3d(tl.routed ? &tmO0 : &tmO1, buf, tl.n0 + 64 * bx, tl.m0 + q * 32,
+                           tl.routed ? tl.seg : 0);
             bulk_commit();
           }
         }
-        if (!ok) break;
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
         continue;
@@ -542,7 +548,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         // plain bf16 store of the [M, N] result
         __nv_bfloat16* orow;
         if (KIND == D2) {
-          orow = out + (int64_t)(tl.out_base + tl.m0 + r) * tl.N;
+          orow = out + (int64_t)(tl.row_base + tl.m0 + r) * tl.N;
         } else {
           const int64_t seg_off = tl.routed ? (int64_t)tl.seg * tl.M * tl.N : 0;
           orow = out + seg_off + (int64_t)(tl.m0 + r) * tl.N;
@@ -573,7 +579,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-    if (Tr::tma_out && threadIdx.x == 64) bulk_wait_all();
+    if (Tr::tma_out && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -585,40 +591,6 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
   }
 }
 
-// ---------------------------------------------------------------- padded layout
-// pad_start[e] = sum_{e' < e} ceil64(kept[e']), pad_start[E] = the total.  One CTA.
-__global__ void pad_plan_kernel(const int32_t* __restrict__ kept, int32_t* __restrict__ pad_start,
-                                int E) {
-  __shared__ int s[kMaxExperts + 1];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s[e] = (kept[e] + 63) & ~63;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      pad_start[e] = acc;
-      acc += s[e];
-    }
-    pad_start[E] = acc;
-  }
-}
-
-// Rows of expert e (blockIdx.y): dst[pad_start[e] + r] = src[expert_start[e] + r] for
-// r < kept[e], zero up to the 64-row boundary.  Rows of vec 16-byte vectors.
-__global__ void pad_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                const int32_t* __restrict__ expert_start,
-                                const int32_t* __restrict__ kept,
-                                const int32_t* __restrict__ pad_start, int vec) {
-  const int e = blockIdx.y;
-  const int n = kept[e], npad = (n + 63) & ~63;
-  const int64_t src0 = expert_start[e], dst0 = pad_start[e];
-  for (int r = blockIdx.x; r < npad; r += gridDim.x) {
-    const int64_t so = (src0 + r) * vec, d = (dst0 + r) * vec;
-    for (int v = threadIdx.x; v < vec; v += blockDim.x)
-      dst[d + v] = r < n ? src[so + v] : make_uint4(0, 0, 0, 0);
-  }
-}
-
-// ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -656,7 +628,7 @@ bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows
   if (!fn) return false;
   const cuuint64_t dims[3] = {cols, rows, segs};
   const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
-  const cuuint32_t box[3] = {64, BM, 1};
+  const cuuint32_t box[3] = {64, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -683,19 +655,15 @@ cudaError_t run(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
 
 }  // namespace
 
-// Rows of the padded routed layout: every segment rounded up to 64 rows.
-static uint64_t padded_rows(const Cfg& c) { return (uint64_t)c.send_rows + 64ull * c.E; }
-
 size_t saved_bytes(const Cfg& c) {
   return 2 * 3 * ((size_t)c.send_rows * c.F + (size_t)c.N * c.Fs);
 }
 
 size_t ffn_backward_ws_bytes(const Cfg& c) {
-  // pad_start [E+1] int32 (256 B aligned); bf16: xpad, dypad [P, d]; gu [P, 2F] +
-  // [N, 2Fs]; h [P, F] + [N, Fs]; dgu [P, 2F] + [N, 2Fs]
-  const size_t P = padded_rows(c), n = (size_t)c.N;
-  const size_t table = ((size_t)(c.E + 1) * 4 + 255) & ~size_t(255);
-  return table + 2 * (P * (2 * (size_t)c.d + 5 * (size_t)c.F) + n * 5 * (size_t)c.Fs);
+  // bf16, send-buffer layout: gu [S, 2F] + [N, 2Fs]; h [S, F] + [N, Fs]; dgu [S, 2F] +
+  // [N, 2Fs]
+  const size_t S = (size_t)c.send_rows, n = (size_t)c.N;
+  return 2 * (S * 5 * (size_t)c.F + n * 5 * (size_t)c.Fs);
 }
 
 cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* expert_start,
@@ -709,44 +677,27 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
   const bool sh = c.Fs > 0;
   const uint64_t N = (uint64_t)c.N, d = (uint64_t)c.d;
   const uint64_t F = (uint64_t)c.F, Fs = (uint64_t)c.Fs, E = (uint64_t)c.E;
-  const uint64_t S = padded_rows(c);  // rows of the padded routed layout
-  int32_t* pad_start = static_cast<int32_t*>(ws);
-  bf* xpad = reinterpret_cast<bf*>(static_cast<char*>(ws) +
-                                   (((size_t)(c.E + 1) * 4 + 255) & ~size_t(255)));
-  bf* dypad = xpad + S * d;
-  bf* gu = dypad + S * d;
+  const uint64_t S = (uint64_t)c.send_rows;  // rows of the send buffer
+  bf* gu = static_cast<bf*>(ws);
   bf* gu_s = gu + S * 2 * F;
   bf* h = gu_s + N * 2 * Fs;
   bf* h_s = h + S * F;
   bf* dgu = h_s + N * Fs;
   bf* dgu_s = dgu + S * 2 * F;
   cudaError_t e;
-  pad_plan_kernel<<<1, 256, 0, s>>>(kept_counts, pad_start, c.E);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const dim3 pgrid(16, c.E);
-  auto pad = [&](const void* src, void* dst, uint64_t cols) {
-    pad_rows_kernel<<<pgrid, 256, 0, s>>>(static_cast<const uint4*>(src),
-                                          static_cast<uint4*>(dst), expert_start, kept_counts,
-                                          pad_start, (int)(cols * 2 / 16));
-    return cudaGetLastError();
-  };
-  if ((e = pad(xperm, xpad, d)) != cudaSuccess) return e;
-  if ((e = pad(dyperm, dypad, d)) != cudaSuccess) return e;
-  BwdParams p{expert_start, kept_counts, pad_start, nullptr, nullptr, nullptr, nullptr, status,
-              c.E, sh ? c.N : 0, c.d, c.F, c.Fs, 0};
+  BwdParams p{expert_start, kept_counts, nullptr, nullptr, nullptr, nullptr, status,
+              c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
   CUtensorMap a0, a1, b0, b1, o0, o1;
-  // activations kept by the forward (moe_expert_ffn_save): h [S, F] + [N, Fs], then
-  // g|u [S_send, 2F] + [N, 2Fs]; otherwise R1 recomputes them in the padded layout
+  // activations kept by the forward (moe_expert_ffn_save), in the send-buffer layout:
+  // h [S, F] + [N, Fs], then g|u [S, 2F] + [N, 2Fs]; otherwise R1 recomputes them
   const bf* sv_h = static_cast<const bf*>(saved);
-  const bf* sv_hs = sv_h ? sv_h + (uint64_t)c.send_rows * F : nullptr;
+  const bf* sv_hs = sv_h ? sv_h + S * F : nullptr;
   const bf* sv_gu = sv_h ? sv_hs + N * Fs : nullptr;
-  const bf* sv_gus = sv_h ? sv_gu + (uint64_t)c.send_rows * 2 * F : nullptr;
-  if (saved) {
-    if ((e = pad(sv_h, h, F)) != cudaSuccess) return e;  // W1 reads h padded
-    p.gu_send_layout = 1;
-  }
-  // R1: A = padded xperm / x (K-major over d); B = W_gu rows (K-major)
-  if (!make_map(&a0, xpad, d, S, 64, BM) || !make_map(&b0, w_gate_up, d, E * 2 * F, 64, BN / 2))
+  const bf* sv_gus = sv_h ? sv_gu + S * 2 * F : nullptr;
+  const bf* hr = saved ? sv_h : h;      // h as W1 reads it
+  const bf* hrs = saved ? sv_hs : h_s;
+  // R1: A = xperm / x (K-major over d); B = W_gu rows (K-major)
+  if (!make_map(&a0, xperm, d, S, 64, BM) || !make_map(&b0, w_gate_up, d, E * 2 * F, 64, BN / 2))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
@@ -754,8 +705,8 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
     return cudaErrorInvalidValue;
   p.out0 = gu; p.out1 = gu_s; p.aux0 = h; p.aux1 = h_s;
   if (!saved && (e = run<R1>(a0, a1, b0, b1, a0, a0, p, s)) != cudaSuccess) return e;
-  // D1: A = padded dY (K-major over d); B = W_down as [d rows, F columns], MN-major
-  if (!make_map(&a0, dypad, d, S, 64, BM) || !make_map(&b0, w_down, F, E * d, 64, 64))
+  // D1: A = dY (K-major over d); B = W_down as [d rows, F columns], MN-major
+  if (!make_map(&a0, dyperm, d, S, 64, BM) || !make_map(&b0, w_down, F, E * d, 64, 64))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
@@ -776,12 +727,12 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
   p.aux0 = p.aux1 = nullptr;
   if ((e = run<D2>(a0, a1, b0, b1, a0, a0, p, s)) != cudaSuccess) return e;
   // W1: dWd[e] = dY_e^T H_e: A = dY MN-major ([rows, d]), B = H MN-major ([rows, F])
-  if (!make_map(&a0, dypad, d, S, 64, 64) || !make_map(&b0, h, F, S, 64, 64))
+  if (!make_map(&a0, dyperm, d, S, 64, 64) || !make_map(&b0, hr, F, S, 64, 64))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
   if (sh && (!make_map(&a1, dout, d, N, 64, 64) ||
-             !make_map(&b1, saved ? sv_hs : h_s, Fs, N, 64, 64)))
+             !make_map(&b1, hrs, Fs, N, 64, 64)))
     return cudaErrorInvalidValue;
   // dWd [E, d, F] and the shared [d, Fs], written by TMA stores
   if (!make_out_map(&o0, dw_down, F, d, E)) return cudaErrorInvalidValue;
@@ -790,7 +741,7 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
   p.out0 = static_cast<bf*>(dw_down); p.out1 = static_cast<bf*>(dshared_down);
   if ((e = run<W1>(a0, a1, b0, b1, o0, o1, p, s)) != cudaSuccess) return e;
   // W2: dW_gu[e] = [dG | dU]_e^T X_e: A = dGU MN-major ([rows, 2F]), B = X MN-major
-  if (!make_map(&a0, dgu, 2 * F, S, 64, 64) || !make_map(&b0, xpad, d, S, 64, 64))
+  if (!make_map(&a0, dgu, 2 * F, S, 64, 64) || !make_map(&b0, xperm, d, S, 64, 64))
     return cudaErrorInvalidValue;
   a1 = a0;
   b1 = b0;
