@@ -84,12 +84,14 @@ struct BwdParams {
   __nv_bfloat16* aux1;  // shared counterpart
   int* err;
   int E, n_shared, d, F, Fs;
+  int padded_layout;  // capacity-padded send buffer: rows between experts never written
 };
 
 struct Ctl {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
   uint32_t tmem_base;
   int abort;
+  int kept_end;  // end of the routed rows written in the send buffer (packed layout)
   int tile_start[MAX_SEG + 1];
   int mtiles[MAX_SEG];
   int rows[MAX_SEG];
@@ -258,7 +260,14 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       if (s < nseg) ctl->tile_start[s] = base + incl - v;
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) ctl->tile_start[nseg] = base;
+    if (lane == 0) {
+      ctl->tile_start[nseg] = base;
+      int end = 0;
+      for (int s = 0; s < p.E; ++s)
+        if (ctl->rows[s] > 0 && ctl->row_base[s] + ctl->rows[s] > end)
+          end = ctl->row_base[s] + ctl->rows[s];
+      ctl->kept_end = end;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -351,16 +360,21 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         int kk_end = BK / 16;  // MMAs (K = 16 each) of this block
         if (Tr::k_rows && tl.routed && k0 + BK > tl.K) {
           // the segment ends inside this block: only the MMAs that reach its rows run,
-          // and the rows past its end inside the last of them (rows rem .. 16*kk_end-1
-          // of every box: 2 of A, 4 of B) are zeroed by the whole warp, whole 128-byte
-          // rows at a time, before the MMA reads them
+          // and the rows past its end inside the last of them (rows rem .. 16*kk_end-1)
+          // are zeroed by the whole warp, whole 128-byte rows at a time, before the MMA
+          // reads them: in A's 2 boxes always (B's rows there are the following
+          // segments', finite values, so their products vanish), in B's 4 boxes too
+          // where those rows may never have been written (past the last written row of
+          // the packed layout, or anywhere in the padded one)
           const int rem = tl.K - k0;
           kk_end = (rem + 15) >> 4;
           const int zr1 = kk_end * 16;
           if (rem < zr1) {
             const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int box = 0; box < 6; ++box) {
+            const bool b_unwritten =
+                p.padded_layout || tl.row_base + k0 + zr1 > ctl->kept_end;
+            const int nbox = b_unwritten ? 6 : 2;
+            for (int box = 0; box < nbox; ++box) {
               uint8_t* base = box < 2 ? sa + box * BOX_BYTES : sa + A_BYTES + (box - 2) * BOX_BYTES;
               for (int row = rem + (lane >> 3); row < zr1; row += 4)
                 *reinterpret_cast<uint4*>(base + row * 128 + (lane & 7) * 16) = z;
@@ -686,7 +700,7 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
   bf* dgu_s = dgu + S * 2 * F;
   cudaError_t e;
   BwdParams p{expert_start, kept_counts, nullptr, nullptr, nullptr, nullptr, status,
-              c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
+              c.E, sh ? c.N : 0, c.d, c.F, c.Fs, c.mode == MOE_DISPATCH_CAPACITY_PADDED ? 1 : 0};
   CUtensorMap a0, a1, b0, b1, o0, o1;
   // activations kept by the forward (moe_expert_ffn_save), in the send-buffer layout:
   // h [S, F] + [N, Fs], then g|u [S, 2F] + [N, 2Fs]; otherwise R1 recomputes them
