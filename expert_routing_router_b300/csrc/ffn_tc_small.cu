@@ -9,14 +9,19 @@
 // the touched experts' weights.  This variant puts a 128-row weight slab on the MMA's
 // M side and the segment's tokens on its N side:
 //   D[128 weight rows][n] = W_slab . X_rows^T,  n = segment rows in the tile rounded
-//   up to 16 (at most 256),
-// and loads tokens in 32-row pieces sized to the segment, so a K step moves 16 KB of
-// weights plus 4 KB per piece instead of 48 KB.  Per CTA (192 threads, persistent,
-// one per SM): warp 0 TMA producer (4-stage ring), warp 1 TMEM owner and MMA issuer,
+//   up to 16 (at most 32 rows per tile; longer segments take several tiles),
+// and loads tokens in 32-row pieces, so a K step moves 16 KB of weights plus 4 KB of
+// tokens instead of 48 KB.  Per CTA (192 threads, persistent, one per SM): warp 0 TMA
+// producer (10-stage ring: the bytes in flight set the streaming rate), warp 1 TMEM
+// owner and MMA issuer,
 // warps 2-5 epilogue.  G1 slab = 64 gate rows + the matching 64 up rows (TMEM lanes
-// 0-63 / 64-127, paired through a small shared-memory exchange); G2 slab = 128 rows
+// 0-63 / 64-127, paired through a small shared-memory exchange); G2 slab = 112 rows
 // of Wd.  Each epilogue thread owns one feature and writes it for 32 tokens at a
-// time.  Every mbarrier wait is bounded (about 2 s, error code in the status word).
+// time.  The down kernel is launched as a programmatic dependent of the gate_up
+// kernel: its CTAs start on the SMs that gate_up CTAs leave, set up, and load their
+// first weight slices before waiting (griddepcontrol.wait) for the gate_up kernel to
+// complete; only then are h rows loaded.  Every mbarrier wait is bounded (about 2 s,
+// error code in the status word).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -29,18 +34,23 @@ namespace {
 using namespace tc;
 
 #ifndef MOE_SMALL_BR
-#define MOE_SMALL_BR 64
+#define MOE_SMALL_BR 32
 #endif
 #ifndef MOE_SMALL_STAGES
-#define MOE_SMALL_STAGES 8
+#define MOE_SMALL_STAGES 10
 #endif
 constexpr int BW = 128;               // weight rows per tile (MMA M, TMEM lanes)
+// Down slabs load 112 weight rows (the MMA still computes 128; TMEM lanes 112-127 are
+// not written out).  A 7168-wide output then splits into 64 slabs per expert instead
+// of 56, which spreads a one-token batch's 9 x 64 tiles over 148 SMs in 3.9 rounds
+// instead of 9 x 56 in 3.4 (4 with a mostly idle last one).
+constexpr int BW2 = 112;
 constexpr int BR = MOE_SMALL_BR;      // token rows per tile (MMA N upper bound)
 constexpr int BK = 64;                // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int STAGES = MOE_SMALL_STAGES;  // deep ring: the step streams weights from DRAM
 constexpr int PIECE = 32;             // token rows per TMA load
 constexpr int PIECE_BYTES = PIECE * BK * 2;
-constexpr int A_BYTES = BW * BK * 2;  // 16 KB weight slab slice
+constexpr int A_BYTES = BW * BK * 2;  // 16 KB weight slab slice (smem room per stage)
 constexpr int B_BYTES = BR * BK * 2;  // token rows slice
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
@@ -112,7 +122,7 @@ __device__ __forceinline__ uint32_t epi_count(bool pred) {
 // G2 128 output features.
 template <int MODE>
 __host__ __device__ constexpr int feat_per_tile() {
-  return MODE == GATE_UP ? BW / 2 : BW;
+  return MODE == GATE_UP ? BW / 2 : BW2;
 }
 
 template <int MODE>
@@ -189,17 +199,30 @@ grouped_ffn_small_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_
   }
   if (warp == 1) tmem_alloc(&ctl->tmem_base, TMEM_COLS);
   if (warp == 2) {  // per-segment tile table
+    // every segment's count and start requested at once (one memory latency), then
+    // the prefix over segments 32 at a time
+    constexpr int CH = (MAX_SEG + 31) / 32;
+    int cnt_r[CH], start_r[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int s = c * 32 + lane;
+      cnt_r[c] = s < p.E ? p.kept_counts[s] : (s == p.E ? p.n_shared : 0);
+      start_r[c] = s < p.E ? p.expert_start[s] : 0;
+    }
     int base = 0;
-    for (int s0 = 0; s0 < nseg; s0 += 32) {
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int s0 = c * 32;
+      if (s0 >= nseg) break;
       const int s = s0 + lane;
       int v = 0;
       if (s < nseg) {
         const bool routed = s < p.E;
-        const int cnt = routed ? p.kept_counts[s] : p.n_shared;
+        const int cnt = cnt_r[c];
         const int rt = (cnt + BR - 1) / BR;
         ctl->rtiles[s] = rt;
         ctl->rows[s] = cnt;
-        ctl->row_base[s] = routed ? p.expert_start[s] : 0;
+        ctl->row_base[s] = start_r[c];
         v = rt * n_slabs<MODE>(routed, p);
       }
       int incl = v;
@@ -218,6 +241,8 @@ grouped_ffn_small_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   const int total = ctl->tile_start[nseg];
+  // the down kernel may be scheduled onto SMs this kernel leaves
+  if (MODE == GATE_UP) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -226,19 +251,29 @@ grouped_ffn_small_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;  // per-stage bits, for the abort drain
       bool ok = true;
+      // down kernel: h comes from the gate_up kernel, whose tail this kernel may overlap
+      // (programmatic launch).  The first tile's weight slices go out for a full ring
+      // at once; its h rows follow griddepcontrol.wait (the gate_up kernel has then
+      // completed and its writes are visible).
+      bool h_ready = MODE == GATE_UP;
+      int npend = 0;  // K steps of the first tile armed without their rows (slots 0..)
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = decode<MODE>(ctl, nseg, t, p);
         const CUtensorMap* mw = tl.routed ? &tmW0 : &tmW1;
         const CUtensorMap* mx = tl.routed ? &tmX0 : &tmX1;
         const int x_row = tl.row_base + tl.r0;
-        const uint32_t bytes = A_BYTES + tl.pieces * PIECE_BYTES;
+        const uint32_t bytes = (MODE == GATE_UP ? A_BYTES : BW2 * BK * 2) + tl.pieces * PIECE_BYTES;
+        auto load_rows = [&](int st, int k) {
+          uint8_t* sb = smem + (size_t)st * STAGE_BYTES + A_BYTES;
+          for (int i = 0; i < tl.pieces; ++i)
+            tma_load(sb + i * PIECE_BYTES, mx, &ctl->full[st], k, x_row + i * PIECE);
+        };
         for (int k0 = 0; k0 < tl.K; k0 += BK) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1, ctl, p.err, 1)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + (size_t)stage * STAGE_BYTES;
-          uint8_t* sb = sa + A_BYTES;
           mbar_expect_tx(&ctl->full[stage], bytes);
           if (MODE == GATE_UP) {
             tma_load(sa, mw, &ctl->full[stage], k0, tl.w_row);
@@ -246,13 +281,19 @@ grouped_ffn_small_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_
           } else {
             tma_load(sa, mw, &ctl->full[stage], k0, tl.w_row);
           }
-          for (int i = 0; i < tl.pieces; ++i)
-            tma_load(sb + i * PIECE_BYTES, mx, &ctl->full[stage], k0, x_row + i * PIECE);
+          if (h_ready) load_rows(stage, k0);
+          else ++npend;
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
+          }
+          if (!h_ready && (npend == STAGES || k0 + BK >= tl.K)) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // h is read by TMA
+            for (int j = 0; j < npend; ++j) load_rows(j, j * BK);
+            h_ready = true;
           }
         }
       }
@@ -368,7 +409,7 @@ grouped_ffn_small_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_
           uint32_t v[32];
           tmem_ld32(tb + (uint32_t)c, v);
           tmem_ld_wait(v);
-          if (f < p.d) {
+          if (lrow < BW2 && f < p.d) {
             const int nj = min(32, tl.rows - c);
             __nv_bfloat16* o = out + (row0 + c) * p.d + f;
 #pragma unroll
@@ -432,8 +473,22 @@ cudaError_t launch(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorM
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     attr_set[dev & 63] = true;
   }
-  kern<<<num_sms(), THREADS, SMEM_BYTES, s>>>(w0, w1, x0, x1, p);
-  return cudaGetLastError();
+  if (MODE == GATE_UP) {
+    kern<<<num_sms(), THREADS, SMEM_BYTES, s>>>(w0, w1, x0, x1, p);
+    return cudaGetLastError();
+  }
+  // the down kernel is a programmatic dependent of the gate_up kernel just before it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, w0, w1, x0, x1, p);
 }
 
 }  // namespace
@@ -459,13 +514,13 @@ cudaError_t launch_ffn_tc_small(const Cfg& c, const void* xperm, const int32_t* 
              c.E, sh ? c.N : 0, c.d, c.F, c.Fs};
   cudaError_t e = launch<GATE_UP>(w0, w1, x0, x1, p, s);
   if (e != cudaSuccess) return e;
-  // G2: weights [E*d, F] / [d, Fs] in 128-row boxes; tokens = h [A, F] / [N, Fs]
-  if (!make_map(&w0, w_down, c.F, (uint64_t)c.E * c.d, BW) ||
+  // G2: weights [E*d, F] / [d, Fs] in 112-row boxes; tokens = h [A, F] / [N, Fs]
+  if (!make_map(&w0, w_down, c.F, (uint64_t)c.E * c.d, BW2) ||
       !make_map(&x0, h_routed, c.F, c.send_rows, PIECE))
     return cudaErrorInvalidValue;
   w1 = w0;
   x1 = x0;
-  if (sh && (!make_map(&w1, shared_down, c.Fs, c.d, BW) ||
+  if (sh && (!make_map(&w1, shared_down, c.Fs, c.d, BW2) ||
              !make_map(&x1, h_shared, c.Fs, c.N, PIECE)))
     return cudaErrorInvalidValue;
   p.out0 = static_cast<__nv_bfloat16*>(yperm);

@@ -421,6 +421,12 @@ EDGE = {
     "small_segments_ragged": small(tokens=40, hidden=264, num_experts=64, top_k=4, num_ranks=8,
                                    num_groups=8, topk_groups=4, capacity_factor=1.0, d_ff=200,
                                    shared_d_ff=72),
+    # the same kernel with skewed routing: two experts with more than one 32-row token
+    # tile (81 rows on the busiest), and a 200-row shared expert (7 token tiles)
+    "small_segments_skewed_row_tiles": small(tokens=200, hidden=264, num_experts=64, top_k=1,
+                                             num_ranks=8, score_fn=0, num_groups=1,
+                                             topk_groups=1, router_offset_std=1.0, d_ff=200,
+                                             shared_d_ff=72, sel_bias_std=0.0),
     "softmax_group_limited": small(tokens=700, hidden=136, num_experts=32, top_k=3, num_ranks=8,
                                    score_fn=0, normalize_topk=False, num_groups=8,
                                    topk_groups=2, d_ff=64, shared_d_ff=0, sel_bias_std=0.0),
