@@ -332,8 +332,10 @@ MOE_API moe_status moe_expert_ffn_save(const moe_config* cfg, const void* xperm,
                                        void* yperm, void* yshared, void* saved, size_t saved_bytes,
                                        void* workspace, size_t workspace_bytes, void* stream);
 
-/* Bytes of the workspace moe_expert_ffn_backward needs (status word, the padded copies
- * of the send rows and of dY, the gate/up and h activations and [dg | du], bf16). */
+/* Bytes of the workspace moe_expert_ffn_backward and moe_route_backward need (one size
+ * serves both): the status word, then the gate/up and h activations and [dg | du]
+ * (bf16, in the send-buffer layout) or the router weight gradient's split logit
+ * gradient and bias partial sums, whichever is larger.  `bytes` is a HOST pointer. */
 MOE_API moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Combine backward.  Same page, step 4, differentiated: for each kept choice,
