@@ -640,8 +640,10 @@ def run_native(a, w, rank, world, local):
         "roofline": {"kernel": "expert grouped GEMMs (gate_up+SwiGLU, down) of moe_expert_ffn",
                      "bound": "tensor", "achieved": ffn_tflops, "peak": pk["bf16"],
                      "unit": "TFLOP/s", "frac": ffn_tflops / pk["bf16"],
-                     "peak_kind": f"{pk['src']} burst bf16 (the timed region is short: SM "
-                                  "clocks stay at their maximum, see clocks)",
+                     "peak_kind": f"{pk['src']} burst bf16 (the 1.1 kW power cap engages "
+                                  "after about six back-to-back steps and slows the later "
+                                  "ones; frac_of_sustained is against the capped figure; "
+                                  "see clocks)",
                      "frac_of_sustained": ffn_tflops / pk["bf16_sust"],
                      "traffic": (measured_ffn_traffic() if w.name == "dsv3_prefill" else None),
                      "traffic_unit": "bytes per moe_expert_ffn call (ncu dram read+write)",
