@@ -276,6 +276,9 @@ __global__ void __launch_bounds__(THREADS, 4)
 select_kernel(const float* __restrict__ partial, int nsplit, int Epad, const float* __restrict__ b,
               const float* __restrict__ sel_bias, float* __restrict__ logits,
               int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteParams p) {
+  // for decode-sized batches a programmatic dependent of the logits kernel: the partial
+  // logits are read only once that kernel has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ float smem[];
   const int E = p.E, EP = E + 1;
   float* lt = smem;
@@ -335,6 +338,8 @@ constexpr int kSmallSelectTokens = 4096;
 __global__ void __launch_bounds__(THREADS)
 route_small_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
                    float* __restrict__ partial, int N, int d, int Epad) {
+  // the selection kernel may be scheduled now: it waits for this one to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float red[THREADS / 32][kSmallRouteTokens];
   const int e = blockIdx.x;
   const int units = d / 8;
@@ -405,8 +410,22 @@ cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, con
   if (c.N <= kSmallSelectTokens) {
     constexpr int TS = 8;
     const size_t sm = (size_t)TS * (c.E + 1) * sizeof(float);
-    select_kernel<TS><<<(c.N + TS - 1) / TS, THREADS, sm, s>>>(
-        partial, nsplit, rp.Epad, b_router, sel_bias, logits, topk_idx, topk_w, p);
+    // decode-sized batches: a programmatic dependent of the logits kernel (its CTAs are
+    // scheduled while that kernel runs and wait for it to complete)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((c.N + TS - 1) / TS);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = c.N <= kSmallRouteTokens ? 1 : 0;
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, select_kernel<TS>, static_cast<const float*>(partial), nsplit,
+                              rp.Epad, b_router, sel_bias, logits, topk_idx, topk_w, p);
   } else {
     if (sm_sel > 48 * 1024)
       cudaFuncSetAttribute(select_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
