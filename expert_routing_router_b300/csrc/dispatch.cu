@@ -208,7 +208,7 @@ assign_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int k, int E, i
               const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ expert_start,
               const int32_t* __restrict__ num_kept, int32_t* __restrict__ slot_of,
               int32_t* __restrict__ perm_src) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // see count_scan_assign
+  pdl_trigger();  // the permute kernel may be scheduled now; it waits for this one
   assign_pass(blockIdx.x, idx, A, N, k, E, C, mode, chunk_base, expert_start, num_kept, slot_of,
               perm_src);
 }
@@ -224,8 +224,7 @@ count_scan_assign_kernel(const int32_t* __restrict__ idx, int64_t A, int N, int 
                          int32_t* __restrict__ rank_offsets, int32_t* __restrict__ num_kept,
                          int32_t* __restrict__ slot_of, int32_t* __restrict__ perm_src,
                          int64_t send_rows) {
-  // the permute kernel may be scheduled now: it waits for this one to complete
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();  // the permute kernel may be scheduled now; it waits for this one
   count_pass(0, 1, idx, A, N, k, E, mode, chunk_hist, perm_src, send_rows);
   __syncthreads();
   scan_pass(chunk_hist, 1, E, R, rank_map, C, mode, expert_counts, kept_counts, expert_start,
@@ -243,9 +242,7 @@ constexpr int UNROLL = 4;
 __global__ void __launch_bounds__(TP)
 permute_kernel(const uint4* __restrict__ x, uint4* __restrict__ xperm,
                const int32_t* __restrict__ slot_of, int N, int k, int nvec) {
-  // launched as a programmatic dependent of the assign pass: its slots are read only
-  // once that pass has completed
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();  // the assign pass has completed: the slots are final
   // a token's slots are loaded one token ahead, so the row copy does not wait on them;
   // a token whose every choice was dropped is not read at all
   int slots[kMaxTopK];
@@ -314,22 +311,12 @@ cudaError_t launch_dispatch(const Cfg& c, const int32_t* topk_idx, const void* x
     const int nvec = (int)((int64_t)c.d * c.act_bytes / 16);
     int grid = num_sms() * 8;
     if (grid > c.N) grid = c.N;
-    // a programmatic dependent of the assign pass: its CTAs are scheduled while that pass
-    // runs, and wait (griddepcontrol.wait) for it to complete before reading the slots
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(TP);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    // a programmatic dependent of the assign pass
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, permute_kernel, static_cast<const uint4*>(x),
-                              static_cast<uint4*>(xperm), static_cast<const int32_t*>(slot_of),
-                              c.N, c.k, nvec);
+    return launch_dependent(permute_kernel, dim3(grid), dim3(TP), 0, s,
+                            static_cast<const uint4*>(x), static_cast<uint4*>(xperm),
+                            static_cast<const int32_t*>(slot_of), c.N, c.k, nvec);
   }
   return cudaGetLastError();
 }

@@ -242,7 +242,7 @@ grouped_ffn_small_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_
   const uint32_t tmem_base = ctl->tmem_base;
   const int total = ctl->tile_start[nseg];
   // the down kernel may be scheduled onto SMs this kernel leaves
-  if (MODE == GATE_UP) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (MODE == GATE_UP) pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -290,7 +290,7 @@ grouped_ffn_small_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_
             phase ^= 1;
           }
           if (!h_ready && (npend == STAGES || k0 + BK >= tl.K)) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");
+            pdl_wait();
             asm volatile("fence.proxy.async.global;" ::: "memory");  // h is read by TMA
             for (int j = 0; j < npend; ++j) load_rows(j, j * BK);
             h_ready = true;
@@ -478,17 +478,8 @@ cudaError_t launch(const CUtensorMap& w0, const CUtensorMap& w1, const CUtensorM
     return cudaGetLastError();
   }
   // the down kernel is a programmatic dependent of the gate_up kernel just before it
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms());
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, w0, w1, x0, x1, p);
+  return launch_dependent(kern, dim3(num_sms()), dim3(THREADS), SMEM_BYTES, s, w0, w1, x0, x1,
+                          p);
 }
 
 }  // namespace

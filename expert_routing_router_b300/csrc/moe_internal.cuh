@@ -180,4 +180,29 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
 // h [S, F] + [N, Fs], then g|u [S, 2F] + [N, 2Fs], bf16.
 size_t saved_bytes(const Cfg& c);
 int num_sms();
+
+// Launch `kern` as a programmatic dependent of the kernel before it on stream `s`: its
+// CTAs may be scheduled while that kernel still runs (once all of that kernel's CTAs
+// have started and executed griddepcontrol.launch_dependents, or exited), so `kern`
+// executes griddepcontrol.wait before it reads anything that kernel writes.  Outside a
+// programmatic launch the wait returns at once.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 }  // namespace moe

@@ -276,9 +276,7 @@ __global__ void __launch_bounds__(THREADS, 4)
 select_kernel(const float* __restrict__ partial, int nsplit, int Epad, const float* __restrict__ b,
               const float* __restrict__ sel_bias, float* __restrict__ logits,
               int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, RouteParams p) {
-  // for decode-sized batches a programmatic dependent of the logits kernel: the partial
-  // logits are read only once that kernel has completed
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();  // decode-sized batches: a dependent of the logits kernel, which has completed
   extern __shared__ float smem[];
   const int E = p.E, EP = E + 1;
   float* lt = smem;
@@ -338,8 +336,7 @@ constexpr int kSmallSelectTokens = 4096;
 __global__ void __launch_bounds__(THREADS)
 route_small_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ W,
                    float* __restrict__ partial, int N, int d, int Epad) {
-  // the selection kernel may be scheduled now: it waits for this one to complete
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();  // the selection kernel may be scheduled now; it waits for this one
   __shared__ float red[THREADS / 32][kSmallRouteTokens];
   const int e = blockIdx.x;
   const int units = d / 8;
@@ -410,29 +407,23 @@ cudaError_t launch_route(const Cfg& c, const void* x, const float* w_router, con
   if (c.N <= kSmallSelectTokens) {
     constexpr int TS = 8;
     const size_t sm = (size_t)TS * (c.E + 1) * sizeof(float);
-    // decode-sized batches: a programmatic dependent of the logits kernel (its CTAs are
-    // scheduled while that kernel runs and wait for it to complete)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((c.N + TS - 1) / TS);
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = sm;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = c.N <= kSmallRouteTokens ? 1 : 0;
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, select_kernel<TS>, static_cast<const float*>(partial), nsplit,
-                              rp.Epad, b_router, sel_bias, logits, topk_idx, topk_w, p);
-  } else {
-    if (sm_sel > 48 * 1024)
-      cudaFuncSetAttribute(select_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sm_sel);
-    select_kernel<TM><<<grid, THREADS, sm_sel, s>>>(partial, nsplit, rp.Epad, b_router, sel_bias,
-                                                    logits, topk_idx, topk_w, p);
+    if (c.N <= kSmallRouteTokens) {
+      // a programmatic dependent of the CUDA-core logits kernel
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      return launch_dependent(select_kernel<TS>, dim3((c.N + TS - 1) / TS), dim3(THREADS), sm,
+                              s, static_cast<const float*>(partial), nsplit, rp.Epad, b_router,
+                              sel_bias, logits, topk_idx, topk_w, p);
+    }
+    select_kernel<TS><<<(c.N + TS - 1) / TS, THREADS, sm, s>>>(
+        partial, nsplit, rp.Epad, b_router, sel_bias, logits, topk_idx, topk_w, p);
+    return cudaGetLastError();
   }
+  if (sm_sel > 48 * 1024)
+    cudaFuncSetAttribute(select_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sm_sel);
+  select_kernel<TM><<<grid, THREADS, sm_sel, s>>>(partial, nsplit, rp.Epad, b_router, sel_bias,
+                                                  logits, topk_idx, topk_w, p);
   return cudaGetLastError();
 }
 
