@@ -427,6 +427,15 @@ EDGE = {
                                              num_ranks=8, score_fn=0, num_groups=1,
                                              topk_groups=1, router_offset_std=1.0, d_ff=200,
                                              shared_d_ff=72, sel_bias_std=0.0),
+    # decode-sized batches on the token-major kernels: no shared expert; and the
+    # capacity-padded layout (each expert's block of C rows at a fixed offset)
+    "small_segments_no_shared": small(tokens=3, hidden=264, num_experts=64, top_k=4,
+                                      num_ranks=8, num_groups=8, topk_groups=4, d_ff=200,
+                                      shared_d_ff=0),
+    "small_segments_padded_bf16": small(tokens=6, hidden=136, num_experts=32, top_k=2,
+                                        num_ranks=4, score_fn=0, num_groups=1, topk_groups=1,
+                                        capacity_factor=1.0, d_ff=72, shared_d_ff=40,
+                                        sel_bias_std=0.0, dispatch_mode=1),
     "softmax_group_limited": small(tokens=700, hidden=136, num_experts=32, top_k=3, num_ranks=8,
                                    score_fn=0, normalize_topk=False, num_groups=8,
                                    topk_groups=2, d_ff=64, shared_d_ff=0, sel_bias_std=0.0),
