@@ -308,8 +308,8 @@ def backward_launches(w):
     """Kernels of this library that one timed backward step launches (the training form:
     g, u and h saved by the forward)."""
     n = 1                      # combine backward
-    n += 4 + 2                 # expert FFN backward: dgrad D1/D2, wgrad W1/W2 on the send
-                               # rows, zeroing of the experts with no rows (dW_gate_up, dW_down)
+    n += 4                     # expert FFN backward: dgrad D1/D2, wgrad W1/W2 on the send
+                               # rows (W1/W2 also write the zero gradients of empty experts)
     n += 2                     # router backward: logit gradient, dx through the router
     n += 4 if (w.act_dtype == "bf16" and w.tokens >= 128) else 1  # dW (split, GEMM, db x2)
     n += 1                     # dispatch backward

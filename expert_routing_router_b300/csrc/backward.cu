@@ -22,7 +22,6 @@
 //                            layers and small batches; bf16 layers from 128 tokens use
 //                            the tensor-core GEMM of router_bwd_tc.cu)
 //   dispatch_bwd_kernel      one CTA per token: the gather-sum above
-//   zero_rows_kernel         zero the weight gradients of experts that received no rows
 #include "moe_internal.cuh"
 #include "sigmoid_fixed.cuh"
 
@@ -355,16 +354,6 @@ dispatch_bwd_kernel(const T* __restrict__ dxperm, const int32_t* __restrict__ sl
 
 // Zero the `per` 16-byte vectors of buf[e] for every expert e with no kept rows:
 // blockIdx.y = expert; CTAs of experts that have rows return at once.
-__global__ void zero_rows_kernel(uint4* __restrict__ buf, const int32_t* __restrict__ kept_counts,
-                                 int64_t per) {
-  const int e = blockIdx.y;
-  if (kept_counts[e] != 0) return;
-  uint4* b = buf + (int64_t)e * per;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < per;
-       i += (int64_t)gridDim.x * blockDim.x)
-    b[i] = make_uint4(0, 0, 0, 0);
-}
-
 int grid_rows(int64_t rows) {
   const int64_t g = (int64_t)num_sms() * 4;
   return (int)(rows < g ? (rows > 0 ? rows : 1) : g);
@@ -429,17 +418,6 @@ cudaError_t launch_dispatch_backward(const Cfg& c, const void* dxperm, const int
         static_cast<const __nv_bfloat16*>(dxperm), slot_of,
         static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(dx_shared),
         dx_router, static_cast<__nv_bfloat16*>(dx), c.N, c.k, c.d);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_zero_empty_experts(const Cfg& c, void* dw_gate_up, void* dw_down,
-                                      const int32_t* kept_counts, cudaStream_t s) {
-  const int64_t per = (int64_t)2 * c.F * c.d * c.act_bytes / 16;  // 16-byte vectors per expert
-  const dim3 grid(32, c.E);
-  zero_rows_kernel<<<grid, TB, 0, s>>>(static_cast<uint4*>(dw_gate_up), kept_counts, per);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  zero_rows_kernel<<<grid, TB, 0, s>>>(static_cast<uint4*>(dw_down), kept_counts, per / 2);
   return cudaGetLastError();
 }
 

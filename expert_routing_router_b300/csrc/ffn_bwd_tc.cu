@@ -28,7 +28,8 @@
 // shared-memory tiles (whole 128-byte rows, so the swizzle does not matter) before the
 // MMA reads them.  The shared expert's rows end where its tensors end, and TMA fills the
 // rest of a block with zeros.
-// Experts with no rows get no W tiles; their gradients are zeroed by a separate kernel.
+// Experts with no rows get no W tiles; their gradients are written as zeros by the W
+// kinds' epilogue warps, interleaved with the tiles (TMA stores of a zeroed box).
 // The W kinds' K loops are short (one segment's rows), so their output write is the
 // critical path: every epilogue warp stages its 32 rows of each 64-column box in shared
 // memory (128-byte swizzle, two alternating 4 KB buffers per warp) and writes it with a
@@ -92,6 +93,8 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
   int kept_end;  // end of the routed rows written in the send buffer (packed layout)
+  int n_empty;   // W kinds: routed experts with no rows, whose gradient is written as zeros
+  int empty_ids[kMaxExperts];
   int tile_start[MAX_SEG + 1];
   int mtiles[MAX_SEG];
   int rows[MAX_SEG];
@@ -101,7 +104,7 @@ struct Ctl {
 template <int KIND>
 constexpr size_t smem_bytes() {
   return 1024 + (size_t)Traits<KIND>::stages * STAGE_BYTES +
-         (Traits<KIND>::tma_out ? OUT_BYTES : 0) + sizeof(Ctl);
+         (Traits<KIND>::tma_out ? OUT_BYTES + WBOX_BYTES : 0) + sizeof(Ctl);
 }
 
 // TMA store of one 64-column x 32-row box of a [segments, M, N] tensor (rows past a
@@ -215,7 +218,8 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stage_out = smem + (size_t)NST * STAGE_BYTES;  // W kinds only
-  Ctl* ctl = reinterpret_cast<Ctl*>(stage_out + (Tr::tma_out ? OUT_BYTES : 0));
+  uint8_t* zero_box = stage_out + OUT_BYTES;               // W kinds: 4 KB of zeros
+  Ctl* ctl = reinterpret_cast<Ctl*>(stage_out + (Tr::tma_out ? OUT_BYTES + WBOX_BYTES : 0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nseg = p.E + (p.n_shared > 0 ? 1 : 0);
 
@@ -267,7 +271,17 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
         if (ctl->rows[s] > 0 && ctl->row_base[s] + ctl->rows[s] > end)
           end = ctl->row_base[s] + ctl->rows[s];
       ctl->kept_end = end;
+      int ne = 0;
+      if (Tr::k_rows)
+        for (int s = 0; s < p.E; ++s)
+          if (ctl->rows[s] == 0) ctl->empty_ids[ne++] = s;
+      ctl->n_empty = ne;
     }
+  }
+  if (Tr::tma_out) {
+    for (int i = threadIdx.x; i < WBOX_BYTES / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(zero_box)[i] = make_uint4(0, 0, 0, 0);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -422,6 +436,31 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // W kinds: the gradients of experts with no rows are zeros, written here as 32-row x
+    // 64-column TMA stores of a zeroed box; the boxes are spread over every epilogue warp
+    // of the grid and issued a few after each tile, while the MMAs of the next run
+    int zn = 0, znbn = 1, zpe = 1, zper = 0, z = 0, zstride = 0;
+    if (Tr::tma_out) {
+      int M, N, K;
+      extents<KIND>(true, 1, p, &M, &N, &K);
+      znbn = (N + 63) / 64;             // boxes across a row of dW
+      zpe = ((M + 31) / 32) * znbn;     // boxes per expert
+      zn = ctl->n_empty * zpe;
+      z = blockIdx.x * 4 + q;
+      zstride = gridDim.x * 4;
+      const int mine = z < zn ? (zn - z + zstride - 1) / zstride : 0;
+      const int tiles = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+      zper = tiles > 0 ? (mine + tiles - 1) / tiles : mine;
+    }
+    auto zero_boxes = [&](int count) {
+      for (int i = 0; i < count && z < zn; ++i, z += zstride) {
+        if (lane == 0) {
+          const int e = ctl->empty_ids[z / zpe], b = z % zpe;
+          tma_store_3d(&tmO0, zero_box, (b % znbn) * 64, (b / znbn) * 32, e);
+          bulk_commit();
+        }
+      }
+    };
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode<KIND>(ctl, nseg, t, p);
       const int Fx = tl.routed ? p.F : p.Fs;
@@ -555,6 +594,7 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
             bulk_commit();
           }
         }
+        zero_boxes(zper);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
         continue;
@@ -593,7 +633,10 @@ ffn_bwd_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-    if (Tr::tma_out && lane == 0) bulk_wait_all();
+    if (Tr::tma_out) {
+      zero_boxes(zn);  // what is left (all of it in a CTA without tiles)
+      if (lane == 0) bulk_wait_all();
+    }
   }
 
   tc_fence_before();
@@ -766,8 +809,7 @@ cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* 
   o1 = o0;
   if (sh && !make_out_map(&o1, dshared_gate_up, d, 2 * Fs, 1)) return cudaErrorInvalidValue;
   p.out0 = static_cast<bf*>(dw_gate_up); p.out1 = static_cast<bf*>(dshared_gate_up);
-  if ((e = run<W2>(a0, a1, b0, b1, o0, o1, p, s)) != cudaSuccess) return e;
-  return launch_zero_empty_experts(c, dw_gate_up, dw_down, kept_counts, s);
+  return run<W2>(a0, a1, b0, b1, o0, o1, p, s);
 }
 
 }  // namespace moe

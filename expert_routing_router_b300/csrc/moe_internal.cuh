@@ -166,8 +166,6 @@ constexpr int kRouterDwTcTokens = 128;
 cudaError_t launch_dispatch_backward(const Cfg& c, const void* dxperm, const int32_t* slot_of,
                                      const void* dout, const void* dx_shared,
                                      const float* dx_router, void* dx, cudaStream_t s);
-cudaError_t launch_zero_empty_experts(const Cfg& c, void* dw_gate_up, void* dw_down,
-                                      const int32_t* kept_counts, cudaStream_t s);
 size_t ffn_backward_ws_bytes(const Cfg& c);
 cudaError_t launch_ffn_backward(const Cfg& c, const void* xperm, const int32_t* expert_start,
                                 const int32_t* kept_counts, const void* w_gate_up,
