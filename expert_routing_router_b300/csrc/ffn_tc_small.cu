@@ -49,6 +49,7 @@ constexpr int BR = MOE_SMALL_BR;      // token rows per tile (MMA N upper bound)
 constexpr int BK = 64;                // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int STAGES = MOE_SMALL_STAGES;  // deep ring: the step streams weights from DRAM
 constexpr int PIECE = 32;             // token rows per TMA load
+static_assert(BR >= PIECE && BR % PIECE == 0 && BR <= 256, "token tile: whole 32-row pieces");
 constexpr int PIECE_BYTES = PIECE * BK * 2;
 constexpr int A_BYTES = BW * BK * 2;  // 16 KB weight slab slice (smem room per stage)
 constexpr int B_BYTES = BR * BK * 2;  // token rows slice
