@@ -469,6 +469,12 @@ EDGE = {
                                                num_ranks=2, score_fn=0, num_groups=1,
                                                topk_groups=1, router_offset_std=0.6,
                                                d_ff=136, shared_d_ff=264, sel_bias_std=0.0),
+    # 128-row-tile kernels with several row tiles on the busiest experts (skewed routing,
+    # about 300 rows per expert), ragged hidden / d_ff, a 1200-row shared expert
+    "skewed_multi_tile_segments": small(tokens=1200, hidden=264, num_experts=4, top_k=1,
+                                          num_ranks=2, score_fn=0, num_groups=1,
+                                          topk_groups=1, router_offset_std=0.8, d_ff=200,
+                                          shared_d_ff=72, sel_bias_std=0.0),
     "capacity_exact_boundary": small(tokens=256, hidden=64, num_experts=4, top_k=1, num_ranks=4,
                                      score_fn=0, num_groups=1, topk_groups=1,
                                      capacity_factor=1.0, d_ff=32, shared_d_ff=0,
