@@ -62,6 +62,10 @@ moe_status make_cfg(const moe_config* in, Cfg* c) {
   if (!std::isfinite(m.capacity_factor)) return MOE_ERR_INVALID_ARG;
   if (m.d_ff < 8 || m.d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
   if (m.shared_d_ff < 0 || m.shared_d_ff % 8 != 0) return MOE_ERR_INVALID_ARG;
+  // weight rows are addressed by 32-bit tensor-map coordinates
+  if ((int64_t)m.num_experts * 2 * m.d_ff > INT32_MAX ||
+      (int64_t)m.num_experts * m.hidden > INT32_MAX || 2 * (int64_t)m.shared_d_ff > INT32_MAX)
+    return MOE_ERR_INVALID_ARG;
   if (m.act_dtype != MOE_DTYPE_F32 && m.act_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (m.dispatch_mode != MOE_DISPATCH_PACKED && m.dispatch_mode != MOE_DISPATCH_CAPACITY_PADDED)
     return MOE_ERR_INVALID_ARG;

@@ -74,7 +74,8 @@ enum { MOE_DISPATCH_PACKED = 0, MOE_DISPATCH_CAPACITY_PADDED = 1 };
  * 1 <= num_ranks <= num_experts (num_experts % num_ranks == 0 for the contiguous
  * map); num_groups divides num_experts; 1 <= topk_groups <= num_groups and
  * topk_groups * (num_experts / num_groups) >= top_k; d_ff >= 8, d_ff % 8 == 0;
- * shared_d_ff == 0 or a multiple of 8. */
+ * shared_d_ff == 0 or a multiple of 8; num_experts * 2 * d_ff, num_experts * hidden
+ * and 2 * shared_d_ff each at most 2^31 - 1 (weight rows take 32-bit coordinates). */
 typedef struct {
   int32_t tokens;          /* N: tokens in the batch */
   int32_t hidden;          /* d: hidden size of a token */

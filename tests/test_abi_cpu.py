@@ -55,7 +55,9 @@ def _route(moe, cfg, ws_bytes=1 << 40, x=FAKE, ws=FAKE, wr=FAKE):
     ("tokens", 0), ("hidden", 12), ("hidden", 4), ("num_experts", 257), ("num_experts", 0),
     ("top_k", 0), ("top_k", 9), ("num_ranks", 0), ("num_ranks", 300), ("rank_map", 2),
     ("score_fn", 3), ("num_groups", 3), ("topk_groups", 9), ("d_ff", 12), ("shared_d_ff", 4),
-    ("act_dtype", 5), ("capacity_factor", float("inf")), ("dispatch_mode", 2)])
+    ("act_dtype", 5), ("capacity_factor", float("inf")), ("dispatch_mode", 2),
+    # 256 experts: more weight rows than 32-bit coordinates reach
+    ("d_ff", 1 << 23), ("hidden", 1 << 23), ("shared_d_ff", 1 << 30)])
 def test_invalid_config_rejected_on_host(moe_lib, field, value):
     cfg = moe_lib.config(W.DSV3_PREFILL)
     setattr(cfg, field, value)
