@@ -20,6 +20,7 @@ its own tokens (weak scaling, no collective on the data path); the time is the m
 over ranks.  --impl reference times the CPU oracle (rank 0 only) on the same metric.
 """
 import argparse
+import datetime
 import json
 import os
 import subprocess
@@ -137,13 +138,16 @@ def weak_scaling_value(tokens_per_rank, steps, world, max_seconds):
 
 # ------------------------------------------------------------------ clocks
 class Clocks:
-    """nvidia-smi sampler running during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampler (every 50 ms).  It starts half a second before the timed
+    region; start() marks where that region begins, and only the samples taken from
+    there to stop() are summarised."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.t0 = None
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
                                        "-lms", "50", "-i", str(index)], stdout=self.f,
@@ -151,6 +155,9 @@ class Clocks:
         except OSError:
             self.p = None
         time.sleep(0.5)
+
+    def start(self):
+        self.t0 = datetime.datetime.now()
 
     def stop(self):
         if self.p is None:
@@ -160,16 +167,33 @@ class Clocks:
         self.f.flush()
         rows = [r.split(", ") for r in open(self.f.name).read().strip().splitlines() if r]
         os.unlink(self.f.name)
-        rows = [r for r in rows if len(r) >= 9]
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = np.array([float(r[1]) for r in rows])
-        mx = float(rows[0][2])
-        load = sm[sm > 0.5 * sm.max()] if sm.size else sm
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
-        return {"sm_mhz": float(np.median(load)), "sm_max_mhz": mx, "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows)}
+        return summarise_clocks(rows, self.t0)
+
+
+CLOCK_REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def summarise_clocks(rows, t0):
+    """Median SM clock, maximum and active throttle reasons over the sampler rows taken
+    at or after t0 (nvidia-smi's local timestamps, the host clock of datetime.now)."""
+    def when(r):
+        try:
+            return datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f")
+        except ValueError:
+            return None
+    rows = [r for r in rows if len(r) >= 10]
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    inside = [r for r in rows if t0 is not None and when(r) is not None and when(r) >= t0]
+    window = "timed region"
+    if not inside:  # a region shorter than the sampling period: the latest sample
+        inside, window = rows[-1:], "last sample (timed region shorter than 50 ms)"
+    sm = np.array([float(r[2]) for r in inside])
+    reasons = sorted({CLOCK_REASONS[i] for r in inside for i in range(4)
+                      if r[6 + i].strip() == "Active"})
+    return {"sm_mhz": float(np.median(sm)), "sm_min_mhz": float(sm.min()),
+            "sm_max_mhz": float(inside[0][3]), "reasons": reasons, "samples": len(inside),
+            "window": window, "power_w_max": max(float(r[4]) for r in inside)}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -535,6 +559,8 @@ def run_native(a, w, rank, world, local):
     clk = Clocks(dev.index) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
+    if clk:
+        clk.start()
     for i in range(a.steps):
         flush.fill_(i & 0xff)            # L2 flush, outside the step's events
         step(runs, evs[i])
@@ -746,6 +772,7 @@ def time_backward(a, w, moe, b, inp, s, flush, pk):
            for _ in range(a.steps)]
     clk = Clocks(dev.index)
     torch.cuda.synchronize()
+    clk.start()
     for i in range(a.steps):
         flush.fill_(i & 0xff)
         evs[i][0].record(s)

@@ -152,3 +152,26 @@ def test_cpu_baseline_sample_never_exceeds_the_batch(tokens):
     assert f"first {n} tokens" in bench.oracle_sample_text(w, n)
     # the per-token part is scaled from the sample to the batch, the rest is not
     assert bench.oracle_rate(w, 1.0, 2.0, tokens) == tokens / 3.0
+
+
+def test_clock_summary_covers_only_the_timed_region():
+    """Samples taken before the timed region (the sampler's start-up, an idle GPU at its
+    top clock) do not enter the median; the throttle reasons are those seen inside it."""
+    import datetime
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5, 500000)
+
+    def row(dt_ms, mhz, cap):
+        ts = (t0 + datetime.timedelta(milliseconds=dt_ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return [ts, "0", str(mhz), "2032", "900.5", "0x4" if cap else "0x0",
+                "Not Active", "Not Active", "Not Active", "Active" if cap else "Not Active"]
+
+    rows = [row(-450, 2032, False), row(-400, 2032, False), row(-50, 2032, False),
+            row(0, 1900, False), row(50, 1400, True), row(100, 1300, True)]
+    c = bench.summarise_clocks(rows, t0)
+    assert c["samples"] == 3 and c["sm_mhz"] == 1400.0 and c["sm_min_mhz"] == 1300.0
+    assert c["sm_max_mhz"] == 2032.0 and c["reasons"] == ["sw_power_cap"]
+    assert c["window"] == "timed region"
+    # a region shorter than the sampling period: the sample that follows it
+    c = bench.summarise_clocks(rows[:3], t0)
+    assert c["samples"] == 1 and c["window"].startswith("last sample")
+    assert bench.summarise_clocks([], t0)["reasons"] == ["no samples"]
